@@ -1,0 +1,231 @@
+/*
+ * nanospec.h — C ABI of the dynamic-vocabulary draft LM head (GB300, sm_103a).
+ *
+ * The library keeps, per sequence, the candidate stream of the NanoSpec /
+ * MicroSpec method resident on the GPU, turns it into the active vocabulary
+ * I_t with a bitmap, packs W_head[I_t, :] into a contiguous buffer and
+ * projects draft hidden states through that sub-head, returning top-k token
+ * ids in the global vocabulary.
+ *
+ * Sources (the paper appears as NanoSpec on one page and as MicroSpec on
+ * another; section numbers are MicroSpec's):
+ *   MicroSpec §3.1 Eq. 1                 z_t = W_head h_t
+ *   MicroSpec §3.2 stream-init equation  S_init = x_{1:L} (+) tuple(U_i T_Kpre(z_i))
+ *   MicroSpec §3.2 stream-update eq.     S_new = S_old (+) tuple(C_draft) (+) tuple(C_ver)
+ *   MicroSpec §3.2 sliding-window eq.    I_{t+1} = Unique(Suffix(S_new, W_max))
+ *   MicroSpec §3.3 "Avoiding Sparse Computation via Asynchronous Gathering"
+ *   MicroSpec §3.3 "Eliminating Overhead via GPU-Resident State Management"
+ *
+ * Conventions for every call:
+ *   - Token ids are 0-based int32 in [0, V).
+ *   - bf16 tensors are passed as uint16_t bit patterns, row-major.
+ *   - Pointers named d_* are DEVICE pointers on the current CUDA device; the
+ *     caller owns them and they are only borrowed for the duration of the
+ *     work the call enqueues.  W_head must stay valid while work that reads
+ *     it is in flight.
+ *   - ns_stream is a cudaStream_t, ns_event a cudaEvent_t (NULL = legacy
+ *     default stream / no event).
+ *   - All calls are asynchronous on the given stream.  No call synchronises
+ *     the host except ns_get_error, ns_create and ns_destroy.  |I_t| stays on
+ *     the device; kernels size themselves from W_max and read the count.
+ *   - A call returns NS_ERR_ARG, without enqueuing anything, when an
+ *     argument is invalid; NS_ERR_CUDA when a CUDA call fails.
+ *   - Device-side problems (an input id outside [0, V)) do not stop the
+ *     stream: the offending entry is skipped and a sticky flag is set, read by
+ *     ns_get_error.
+ *   - Work for one sequence must be ordered (one stream, or events).  Work
+ *     for different sequences may run concurrently.
+ *   - Logits must be finite; the order among NaNs is undefined.
+ */
+#ifndef NANOSPEC_H
+#define NANOSPEC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Entry points are exported even when the library is built with hidden
+ * default visibility. */
+#if defined(__GNUC__)
+#define NS_API __attribute__((visibility("default")))
+#else
+#define NS_API
+#endif
+
+typedef int32_t ns_status;
+#define NS_OK 0
+#define NS_ERR_ARG (-1)     /* invalid argument; nothing enqueued            */
+#define NS_ERR_CUDA (-2)    /* a CUDA runtime call or launch failed          */
+#define NS_ERR_OOM (-3)     /* device allocation failed                      */
+#define NS_ERR_TIMEOUT (-4) /* a bounded device-side wait ran out            */
+#define NS_ERR_STATE (-5)   /* call out of order (e.g. append before init)   */
+
+/* Sticky device error flags (bit mask), read with ns_get_error. */
+#define NS_FLAG_BAD_ID 0x1u    /* an input token id outside [0, V) was skipped */
+#define NS_FLAG_OVERFLOW 0x2u  /* an internal capacity was exceeded (bug)      */
+#define NS_FLAG_TIMEOUT 0x4u   /* a bounded device-side wait gave up            */
+
+typedef void *ns_stream; /* cudaStream_t */
+typedef void *ns_event;  /* cudaEvent_t  */
+
+/* Limits of this build. */
+#define NS_MAX_SELECT_K 16 /* K_pre and K_ver                               */
+#define NS_MAX_TOPK 32     /* k of the sub-head top-k                       */
+#define NS_MAX_ROWS 64     /* hidden rows per projection call (draft nodes) */
+
+typedef struct ns_config {
+  int32_t V;          /* vocabulary size (rows of W_head), >= 1               */
+  int32_t H;          /* hidden size d (columns of W_head), multiple of 64    */
+  int32_t W_max;      /* sliding-window length, >= 1                          */
+  int32_t K_pre;      /* Top-K per prefill row, 0..NS_MAX_SELECT_K            */
+  int32_t K_ver;      /* Top-K of the verify row, 0..NS_MAX_SELECT_K          */
+  int32_t max_tree;   /* most draft-tree ids per append, 0..NS_MAX_ROWS       */
+  int32_t max_k;      /* most top-k per hidden row, 1..NS_MAX_TOPK            */
+  int32_t batch;      /* independent sequences, >= 1                          */
+  int32_t max_prompt; /* longest prompt accepted by ns_stream_init, >= 1      */
+} ns_config;
+
+typedef struct ns_handle ns_handle;
+
+/* Returns a static, human-readable name of a status code. */
+NS_API const char *ns_status_string(ns_status s);
+
+/*
+ * Allocates all device state for cfg->batch sequences on the current device
+ * (per sequence: ring of W_max int32 stream entries, V occurrence counts,
+ * ceil(V/32) bitmap words, I_t as W_max int32 + count, the packed sub-head
+ * W_max x H bf16 — MicroSpec §3.3's pre-allocated contiguous buffer — and
+ * scratch).  The state starts empty; every sequence must be initialised with
+ * ns_stream_init before it is appended to.  Synchronises the device.
+ * *out receives the handle; NS_ERR_ARG on bad limits, NS_ERR_OOM when
+ * allocation fails.
+ */
+NS_API ns_status ns_create(const ns_config *cfg, ns_handle **out);
+
+/* Synchronises the device and frees everything the handle owns. */
+NS_API ns_status ns_destroy(ns_handle *h);
+
+/* Bytes of device memory the handle holds (all sequences). */
+NS_API int64_t ns_device_bytes(const ns_handle *h);
+
+/*
+ * Prefill: S_init = prompt (+) tuple(union over i of T_Kpre(z_i))
+ * (MicroSpec §3.2, stream-initialisation equation).
+ *   d_prompt          int32 [L], 1 <= L <= max_prompt, ids in [0, V)
+ *   d_prefill_logits  fp32 [L x V] row-major, row i = z_i (may be NULL when
+ *                     K_pre == 0)
+ * The union is deduplicated in first-occurrence order, position-major then
+ * rank-minor (largest logit first, ties to the smaller id); prompt ids are
+ * kept verbatim.  Only the last W_max entries of S_init are stored.  Resets
+ * the sequence's previous state.  Out-of-range prompt ids are skipped and
+ * flag NS_FLAG_BAD_ID.  Leaves I_t unbuilt (call ns_build_active_vocab).
+ */
+NS_API ns_status ns_stream_init(ns_handle *h, int32_t seq, const int32_t *d_prompt, int32_t L,
+                         const float *d_prefill_logits, ns_stream stream);
+
+/*
+ * Decode-step update S_new = S_old (+) tuple(C_draft) (+) tuple(C_ver)
+ * (MicroSpec §3.2, "Dynamic Stream Update" and the stream-update equation),
+ * then the window counts and bitmap of Unique(Suffix(S_new, W_max)).
+ *   d_tree_ids       int32 [n_tree], 0 <= n_tree <= max_tree: every node of
+ *                    the draft tree; C_draft = distinct ids in first-occurrence
+ *                    node order (out-of-range ids skipped, NS_FLAG_BAD_ID)
+ *   d_verify_logits  fp32 [n_verify x V] row-major; C_ver = T_Kver of row
+ *                    verify_row (value descending, ties to the smaller id).
+ *                    May be NULL when K_ver == 0.
+ * Everything appended refreshes recency; entries older than the last W_max
+ * are evicted.  Does not rebuild I_t.
+ */
+NS_API ns_status ns_stream_append(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
+                           const float *d_verify_logits, int32_t n_verify, int32_t verify_row,
+                           ns_stream stream);
+
+/*
+ * I_t = Unique(Suffix(S, W_max)) read out of the bitmap in ascending id order
+ * (MicroSpec §3.2 sliding-window equation; §3.3 GPU-resident bitmaps).
+ * Writes the device list and its device count (see ns_get_active).
+ */
+NS_API ns_status ns_build_active_vocab(ns_handle *h, int32_t seq, ns_stream stream);
+
+/*
+ * packed[j, :] = W_head[I_t[j], :] for j < |I_t| (MicroSpec §3.3, gathering
+ * into the pre-allocated contiguous buffer).  Meant for a copy stream that
+ * overlaps the draft backbone: when `done` is not NULL it is recorded on
+ * copy_stream after the gather, and the projection's stream should wait on
+ * it.  d_W_head: bf16 [V x H] row-major.
+ */
+NS_API ns_status ns_gather_head_rows(ns_handle *h, int32_t seq, const uint16_t *d_W_head,
+                              ns_stream copy_stream, ns_event done);
+
+/*
+ * Sub-head projection and top-k on the packed buffer:
+ *   logits[r, j] = sum_h hidden[r, h] * packed[j, h]   (Eq. 1 on W_head[I_t,:]),
+ * bf16 inputs, fp32 accumulation, for r < n, j < |I_t|; then per row the k
+ * largest logits (ties to the smaller id) mapped to global ids I_t[j].
+ *   d_hidden     bf16 [n x H], 1 <= n <= NS_MAX_ROWS
+ *   k            1 <= k <= max_k
+ *   d_logits     fp32 [n x ld_logits] or NULL; columns >= |I_t| untouched;
+ *                ld_logits >= W_max
+ *   d_topk_ids   int32 [n x k]; rows with |I_t| < k are padded with -1
+ *   d_topk_vals  fp32  [n x k]; padding is -inf
+ */
+NS_API ns_status ns_sub_lm_head_logits_topk(ns_handle *h, int32_t seq, const uint16_t *d_hidden, int32_t n,
+                                     int32_t k, float *d_logits, int32_t ld_logits,
+                                     int32_t *d_topk_ids, float *d_topk_vals, ns_stream stream);
+
+/*
+ * One whole decode step for one sequence, in as few launches as the library
+ * can: ns_stream_append, ns_build_active_vocab, the gather (writing the
+ * packed buffer) and the projection with top-k, with the same arguments and
+ * results as those calls made in order on `stream`.
+ */
+NS_API ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
+                  const float *d_verify_logits, int32_t n_verify, int32_t verify_row,
+                  const uint16_t *d_W_head, const uint16_t *d_hidden, int32_t n, int32_t k,
+                  float *d_logits, int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
+                  ns_stream stream);
+
+/*
+ * Dense head on a fixed row range: logits over rows [0, rows) of W_head
+ * (rows = V is the full-vocabulary LM head of Eq. 1; rows = 32768 a static
+ * frequency-ranked sub-head) and per-row top-k with ids = row numbers.
+ * Uses the handle's dense scratch (sized for V rows); the handle's V and H
+ * bound `rows` and fix H.  Arguments as in ns_sub_lm_head_logits_topk;
+ * ld_logits >= rows when d_logits is not NULL.
+ */
+NS_API ns_status ns_dense_lm_head_topk(ns_handle *h, const uint16_t *d_W_head, int32_t rows,
+                                const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
+                                int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
+                                ns_stream stream);
+
+/*
+ * Device pointers into a sequence's state (owned by the handle; valid until
+ * ns_destroy).  Any out-pointer may be NULL.
+ *   ids     int32 [W_max]  I_t ascending (first *count entries valid)
+ *   count   int32 [1]      |I_t|
+ *   bitmap  uint32 [ceil(V/32)]  bit (i % 32) of word i / 32 set iff i in window
+ *   packed  bf16 [W_max x H]     rows j < |I_t| valid after a gather
+ */
+NS_API ns_status ns_get_active(ns_handle *h, int32_t seq, const int32_t **ids, const int32_t **count,
+                        const uint32_t **bitmap, const uint16_t **packed);
+
+/*
+ * Device pointers to the raw stream state (for inspection and tests):
+ *   ring    int32 [W_max]  stream entry at position p lives at ring[p % W_max]
+ *   length  int64 [1]      total number of entries ever appended (|S|)
+ *   counts  uint32 [V]     occurrences of each id among the last W_max entries
+ */
+NS_API ns_status ns_get_state(ns_handle *h, int32_t seq, const int32_t **ring, const int64_t **length,
+                       const uint32_t **counts);
+
+/* Synchronises the device, returns the sticky NS_FLAG_* mask, and clears it
+ * when `clear` is non-zero. */
+NS_API ns_status ns_get_error(ns_handle *h, uint32_t *flags, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NANOSPEC_H */

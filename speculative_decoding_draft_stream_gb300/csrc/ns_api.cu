@@ -1,0 +1,329 @@
+// C ABI of the dynamic-vocabulary draft LM head (declared in include/nanospec.h).
+//
+// The handle owns one device allocation holding every sequence's state
+// (MicroSpec §3.3: all window state resident in VRAM, a pre-allocated
+// contiguous buffer for the packed sub-head) plus scratch.  Calls validate
+// their arguments on the host, then only enqueue kernels on the caller's
+// stream: no host synchronisation and no allocation after ns_create.
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "ns_internal.cuh"
+
+struct ns_handle {
+  ns_config cfg;
+  ns::Dims dims;
+  int device = 0;
+  int num_sms = 0;
+  int vgrid = 1;  // CTAs of the verify Top-K
+  int pgrid = 1;  // CTAs of the projection
+  int ggrid = 1;  // CTAs of the gather
+  char *base = nullptr;
+  size_t bytes = 0;
+  uint32_t *err = nullptr;
+  std::vector<ns::SeqDev> seqs;
+  std::vector<char> inited;
+  float *dense_logits = nullptr;  // [kProjBN x dense_ld]
+  float *dense_part = nullptr;    // [pgrid x tile]
+  int32_t *dense_tickets = nullptr;
+  int dense_ld = 0;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxV = 524288;  // one CTA compacts the bitmap (4 uint4 words per thread)
+constexpr int kMaxH = 8192;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+// Two passes over the same layout: the first (base == nullptr) only sums sizes.
+struct Carver {
+  char *base;
+  size_t off = 0;
+  explicit Carver(char *b) : base(b) {}
+  template <typename T>
+  T *take(size_t count) {
+    T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+    off += align_up(count * sizeof(T) + (count == 0 ? 1 : 0));
+    return p;
+  }
+};
+
+void layout(ns_handle *h, Carver &cv) {
+  const ns_config &c = h->cfg;
+  const ns::Dims &d = h->dims;
+  h->err = cv.take<uint32_t>(1);
+  h->seqs.assign(c.batch, ns::SeqDev{});
+  for (int b = 0; b < c.batch; ++b) {
+    ns::SeqDev &s = h->seqs[b];
+    s.ring = cv.take<int32_t>(c.W_max);
+    s.counts = cv.take<uint32_t>(c.V);
+    s.bitmap = cv.take<uint32_t>(d.nwords_pad);
+    s.active = cv.take<int32_t>(c.W_max);
+    s.count = cv.take<int32_t>(1);
+    s.length = cv.take<long long>(1);
+    s.packed = cv.take<uint16_t>((size_t)c.W_max * c.H);
+    s.logits = cv.take<float>((size_t)ns::kProjBN * d.ld_scratch);
+    s.vpart_v = cv.take<float>((size_t)h->vgrid * NS_MAX_SELECT_K);
+    s.vpart_i = cv.take<int32_t>((size_t)h->vgrid * NS_MAX_SELECT_K);
+    s.vticket = cv.take<int32_t>(1);
+    s.ppart = cv.take<float>((size_t)h->pgrid * ns::kProjBN * ns::kProjBM);
+    s.pticket = cv.take<int32_t>(h->pgrid);
+    s.first = c.K_pre > 0 ? cv.take<int32_t>(c.V) : nullptr;
+    s.cand = c.K_pre > 0 ? cv.take<int32_t>((size_t)c.max_prompt * c.K_pre) : nullptr;
+    s.sinit = cv.take<int32_t>((size_t)c.max_prompt * (1 + c.K_pre));
+  }
+  h->dense_ld = (c.V + 3) & ~3;
+  h->dense_logits = cv.take<float>((size_t)ns::kProjBN * h->dense_ld);
+  h->dense_part = cv.take<float>((size_t)h->pgrid * ns::kProjBN * ns::kProjBM);
+  h->dense_tickets = cv.take<int32_t>(h->pgrid);
+}
+
+bool valid_seq(const ns_handle *h, int32_t seq) { return h && seq >= 0 && seq < h->cfg.batch; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+ns_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NS_OK : NS_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *ns_status_string(ns_status s) {
+  switch (s) {
+    case NS_OK: return "ok";
+    case NS_ERR_ARG: return "invalid argument";
+    case NS_ERR_CUDA: return "CUDA error";
+    case NS_ERR_OOM: return "out of device memory";
+    case NS_ERR_TIMEOUT: return "device wait timed out";
+    case NS_ERR_STATE: return "call out of order";
+    default: return "unknown status";
+  }
+}
+
+ns_status ns_create(const ns_config *cfg, ns_handle **out) {
+  if (!cfg || !out) return NS_ERR_ARG;
+  *out = nullptr;
+  const ns_config c = *cfg;
+  if (c.V < 1 || c.V > kMaxV || c.H < 64 || c.H > kMaxH || c.H % 64 != 0 || c.W_max < 1 ||
+      c.W_max > (1 << 20) || c.K_pre < 0 || c.K_pre > NS_MAX_SELECT_K || c.K_pre > c.V || c.K_ver < 0 ||
+      c.K_ver > NS_MAX_SELECT_K || c.K_ver > c.V || c.max_tree < 0 || c.max_tree > NS_MAX_ROWS || c.max_k < 1 ||
+      c.max_k > NS_MAX_TOPK || c.batch < 1 || c.batch > 4096 || c.max_prompt < 1 || c.max_prompt > (1 << 20))
+    return NS_ERR_ARG;
+  ns_handle *h = new (std::nothrow) ns_handle();
+  if (!h) return NS_ERR_OOM;
+  h->cfg = c;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
+      ns::prepare_project_kernels() != cudaSuccess) {
+    delete h;
+    return NS_ERR_CUDA;
+  }
+  ns::Dims &d = h->dims;
+  d.V = c.V;
+  d.H = c.H;
+  d.W_max = c.W_max;
+  d.K_pre = c.K_pre;
+  d.K_ver = c.K_ver;
+  d.nwords = (c.V + 31) / 32;
+  d.nwords_pad = (d.nwords + 3) & ~3;
+  d.ld_scratch = (c.W_max + 3) & ~3;
+  const int per_cta = 4 * ns::kStateThreads;  // one float4 per thread
+  h->vgrid = (c.V + per_cta - 1) / per_cta;
+  if (h->vgrid > h->num_sms) h->vgrid = h->num_sms;
+  h->pgrid = 2 * h->num_sms;
+  h->ggrid = 4 * h->num_sms;
+
+  Carver sizing(nullptr);
+  layout(h, sizing);
+  h->bytes = sizing.off;
+  if (cudaMalloc(reinterpret_cast<void **>(&h->base), h->bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return NS_ERR_OOM;
+  }
+  Carver carve(h->base);
+  layout(h, carve);
+  if (cudaMemset(h->base, 0, h->bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(h->base);
+    delete h;
+    return NS_ERR_CUDA;
+  }
+  h->inited.assign(c.batch, 0);
+  *out = h;
+  return NS_OK;
+}
+
+ns_status ns_destroy(ns_handle *h) {
+  if (!h) return NS_ERR_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (h->base) cudaFree(h->base);
+  delete h;
+  return cuda_status(e);
+}
+
+int64_t ns_device_bytes(const ns_handle *h) { return h ? (int64_t)h->bytes : 0; }
+
+ns_status ns_stream_init(ns_handle *h, int32_t seq, const int32_t *d_prompt, int32_t L,
+                         const float *d_prefill_logits, ns_stream stream) {
+  if (!valid_seq(h, seq) || !d_prompt || L < 1 || L > h->cfg.max_prompt) return NS_ERR_ARG;
+  if (h->cfg.K_pre > 0 && !d_prefill_logits) return NS_ERR_ARG;
+  ns_status st = cuda_status(ns::launch_init(h->seqs[seq], h->dims, d_prompt, L, d_prefill_logits, h->err,
+                                             static_cast<cudaStream_t>(stream)));
+  if (st == NS_OK) h->inited[seq] = 1;
+  return st;
+}
+
+static ns_status check_append_args(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
+                                   const float *d_verify_logits, int32_t n_verify, int32_t verify_row) {
+  if (!valid_seq(h, seq) || n_tree < 0 || n_tree > h->cfg.max_tree || (n_tree > 0 && !d_tree_ids))
+    return NS_ERR_ARG;
+  if (h->cfg.K_ver > 0 && (!d_verify_logits || n_verify < 1 || verify_row < 0 || verify_row >= n_verify))
+    return NS_ERR_ARG;
+  if (!h->inited[seq]) return NS_ERR_STATE;
+  return NS_OK;
+}
+
+ns_status ns_stream_append(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
+                           const float *d_verify_logits, int32_t n_verify, int32_t verify_row, ns_stream stream) {
+  ns_status st = check_append_args(h, seq, d_tree_ids, n_tree, d_verify_logits, n_verify, verify_row);
+  if (st != NS_OK) return st;
+  const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
+  return cuda_status(ns::launch_append(h->seqs[seq], h->dims, h->vgrid, d_tree_ids, n_tree, zrow, false, h->err,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+ns_status ns_build_active_vocab(ns_handle *h, int32_t seq, ns_stream stream) {
+  if (!valid_seq(h, seq)) return NS_ERR_ARG;
+  if (!h->inited[seq]) return NS_ERR_STATE;
+  return cuda_status(ns::launch_build(h->seqs[seq], h->dims, h->err, static_cast<cudaStream_t>(stream)));
+}
+
+ns_status ns_gather_head_rows(ns_handle *h, int32_t seq, const uint16_t *d_W_head, ns_stream copy_stream,
+                              ns_event done) {
+  if (!valid_seq(h, seq) || !d_W_head || !aligned16(d_W_head)) return NS_ERR_ARG;
+  if (!h->inited[seq]) return NS_ERR_STATE;
+  cudaStream_t st = static_cast<cudaStream_t>(copy_stream);
+  cudaError_t e = ns::launch_gather(h->seqs[seq], h->dims, d_W_head, h->ggrid, st);
+  if (e == cudaSuccess && done) e = cudaEventRecord(static_cast<cudaEvent_t>(done), st);
+  return cuda_status(e);
+}
+
+static ns_status check_proj_args(ns_handle *h, const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
+                                 int32_t ld_logits, int32_t min_ld, int32_t *d_ids, float *d_vals) {
+  if (!d_hidden || !aligned16(d_hidden) || n < 1 || n > NS_MAX_ROWS || k < 1 || k > h->cfg.max_k || !d_ids ||
+      !d_vals)
+    return NS_ERR_ARG;
+  if (d_logits && ld_logits < min_ld) return NS_ERR_ARG;
+  return NS_OK;
+}
+
+ns_status ns_sub_lm_head_logits_topk(ns_handle *h, int32_t seq, const uint16_t *d_hidden, int32_t n, int32_t k,
+                                     float *d_logits, int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
+                                     ns_stream stream) {
+  if (!valid_seq(h, seq)) return NS_ERR_ARG;
+  ns_status st = check_proj_args(h, d_hidden, n, k, d_logits, ld_logits, h->cfg.W_max, d_topk_ids, d_topk_vals);
+  if (st != NS_OK) return st;
+  if (!h->inited[seq]) return NS_ERR_STATE;
+  const ns::SeqDev &s = h->seqs[seq];
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  ns::ProjArgs a{};
+  a.rows = s.packed;
+  a.count_ptr = s.count;
+  a.hid = d_hidden;
+  a.n = n;
+  a.H = h->cfg.H;
+  a.logits = d_logits ? d_logits : s.logits;
+  a.ld = d_logits ? ld_logits : h->dims.ld_scratch;
+  a.part = s.ppart;
+  a.tickets = s.pticket;
+  cudaError_t e = ns::launch_project(ns::kFromPacked, a, h->pgrid, cs);
+  if (e == cudaSuccess) e = ns::launch_topk(a.logits, a.ld, s.count, 0, s.active, n, k, d_topk_ids, d_topk_vals, cs);
+  return cuda_status(e);
+}
+
+ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
+                  const float *d_verify_logits, int32_t n_verify, int32_t verify_row, const uint16_t *d_W_head,
+                  const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits, int32_t ld_logits,
+                  int32_t *d_topk_ids, float *d_topk_vals, ns_stream stream) {
+  ns_status st = check_append_args(h, seq, d_tree_ids, n_tree, d_verify_logits, n_verify, verify_row);
+  if (st != NS_OK) return st;
+  if (!d_W_head || !aligned16(d_W_head)) return NS_ERR_ARG;
+  st = check_proj_args(h, d_hidden, n, k, d_logits, ld_logits, h->cfg.W_max, d_topk_ids, d_topk_vals);
+  if (st != NS_OK) return st;
+  const ns::SeqDev &s = h->seqs[seq];
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
+  cudaError_t e = ns::launch_append(s, h->dims, h->vgrid, d_tree_ids, n_tree, zrow, true, h->err, cs);
+  if (e != cudaSuccess) return NS_ERR_CUDA;
+  ns::ProjArgs a{};
+  a.rows = d_W_head;
+  a.idx = s.active;
+  a.count_ptr = s.count;
+  a.packed_out = s.packed;
+  a.hid = d_hidden;
+  a.n = n;
+  a.H = h->cfg.H;
+  a.logits = d_logits ? d_logits : s.logits;
+  a.ld = d_logits ? ld_logits : h->dims.ld_scratch;
+  a.part = s.ppart;
+  a.tickets = s.pticket;
+  e = ns::launch_project(ns::kGatherRows, a, h->pgrid, cs);
+  if (e == cudaSuccess) e = ns::launch_topk(a.logits, a.ld, s.count, 0, s.active, n, k, d_topk_ids, d_topk_vals, cs);
+  return cuda_status(e);
+}
+
+ns_status ns_dense_lm_head_topk(ns_handle *h, const uint16_t *d_W_head, int32_t rows, const uint16_t *d_hidden,
+                                int32_t n, int32_t k, float *d_logits, int32_t ld_logits, int32_t *d_topk_ids,
+                                float *d_topk_vals, ns_stream stream) {
+  if (!h || !d_W_head || !aligned16(d_W_head) || rows < 1 || rows > h->cfg.V) return NS_ERR_ARG;
+  ns_status st = check_proj_args(h, d_hidden, n, k, d_logits, ld_logits, rows, d_topk_ids, d_topk_vals);
+  if (st != NS_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  ns::ProjArgs a{};
+  a.rows = d_W_head;
+  a.rows_host = rows;
+  a.hid = d_hidden;
+  a.n = n;
+  a.H = h->cfg.H;
+  a.logits = d_logits ? d_logits : h->dense_logits;
+  a.ld = d_logits ? ld_logits : h->dense_ld;
+  a.part = h->dense_part;
+  a.tickets = h->dense_tickets;
+  cudaError_t e = ns::launch_project(ns::kDenseRows, a, h->pgrid, cs);
+  if (e == cudaSuccess) e = ns::launch_topk(a.logits, a.ld, nullptr, rows, nullptr, n, k, d_topk_ids, d_topk_vals, cs);
+  return cuda_status(e);
+}
+
+ns_status ns_get_active(ns_handle *h, int32_t seq, const int32_t **ids, const int32_t **count,
+                        const uint32_t **bitmap, const uint16_t **packed) {
+  if (!valid_seq(h, seq)) return NS_ERR_ARG;
+  const ns::SeqDev &s = h->seqs[seq];
+  if (ids) *ids = s.active;
+  if (count) *count = s.count;
+  if (bitmap) *bitmap = s.bitmap;
+  if (packed) *packed = s.packed;
+  return NS_OK;
+}
+
+ns_status ns_get_state(ns_handle *h, int32_t seq, const int32_t **ring, const int64_t **length,
+                       const uint32_t **counts) {
+  if (!valid_seq(h, seq)) return NS_ERR_ARG;
+  const ns::SeqDev &s = h->seqs[seq];
+  if (ring) *ring = s.ring;
+  if (length) *length = reinterpret_cast<const int64_t *>(s.length);
+  if (counts) *counts = s.counts;
+  return NS_OK;
+}
+
+ns_status ns_get_error(ns_handle *h, uint32_t *flags, int32_t clear) {
+  if (!h || !flags) return NS_ERR_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(flags, h->err, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(h->err, 0, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) e = cudaDeviceSynchronize();
+  return cuda_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,253 @@
+"""ctypes binding of libnanospec.so (include/nanospec.h), same names as the C ABI.
+
+This module only marshals arguments: torch tensors become device pointers and
+CUDA stream/event handles, and status codes become exceptions.  Every step of
+the method runs in the library's CUDA kernels.  There is no fallback: if the
+library is missing or cannot be loaded, loading raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "libnanospec.so")
+
+NS_OK = 0
+STATUS_NAMES = {0: "NS_OK", -1: "NS_ERR_ARG", -2: "NS_ERR_CUDA", -3: "NS_ERR_OOM", -4: "NS_ERR_TIMEOUT",
+                -5: "NS_ERR_STATE"}
+FLAG_BAD_ID = 0x1
+FLAG_OVERFLOW = 0x2
+FLAG_TIMEOUT = 0x4
+MAX_SELECT_K = 16
+MAX_TOPK = 32
+MAX_ROWS = 64
+
+# Every entry point declared in include/nanospec.h.
+EXPORTED = (
+    "ns_status_string", "ns_create", "ns_destroy", "ns_device_bytes", "ns_stream_init", "ns_stream_append",
+    "ns_build_active_vocab", "ns_gather_head_rows", "ns_sub_lm_head_logits_topk", "ns_step",
+    "ns_dense_lm_head_topk", "ns_get_active", "ns_get_state", "ns_get_error",
+)
+
+
+class NanoSpecError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class ns_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("V", "H", "W_max", "K_pre", "K_ver", "max_tree", "max_k", "batch", "max_prompt")]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads the library (once).  Raises OSError when it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise OSError(f"{path} not found: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    P, I32, I64, U16P = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    sig = {
+        "ns_status_string": (ctypes.c_char_p, [I32]),
+        "ns_create": (I32, [ctypes.POINTER(ns_config), ctypes.POINTER(P)]),
+        "ns_destroy": (I32, [P]),
+        "ns_device_bytes": (I64, [P]),
+        "ns_stream_init": (I32, [P, I32, P, I32, P, P]),
+        "ns_stream_append": (I32, [P, I32, P, I32, P, I32, I32, P]),
+        "ns_build_active_vocab": (I32, [P, I32, P]),
+        "ns_gather_head_rows": (I32, [P, I32, U16P, P, P]),
+        "ns_sub_lm_head_logits_topk": (I32, [P, I32, U16P, I32, I32, P, I32, P, P, P]),
+        "ns_step": (I32, [P, I32, P, I32, P, I32, I32, U16P, U16P, I32, I32, P, I32, P, P, P]),
+        "ns_dense_lm_head_topk": (I32, [P, U16P, I32, U16P, I32, I32, P, I32, P, P, P]),
+        "ns_get_active": (I32, [P, I32, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P),
+                                ctypes.POINTER(P)]),
+        "ns_get_state": (I32, [P, I32, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P)]),
+        "ns_get_error": (I32, [P, ctypes.POINTER(ctypes.c_uint32), I32]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != NS_OK:
+        raise NanoSpecError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, what: str = "tensor") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{what} has dtype {t.dtype}, expected {dtype}")
+    return t.data_ptr()
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        s = torch.cuda.current_stream()
+    return s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+
+
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (torch.bfloat16, torch.int16)
+
+
+class _DevView:
+    """Object exposing a raw device pointer through __cuda_array_interface__."""
+
+    def __init__(self, ptr: int, shape, typestr: str):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr, False),
+                                         "version": 3, "strides": None}
+
+
+def _view(ptr: int, shape, typestr: str, device) -> torch.Tensor:
+    return torch.as_tensor(_DevView(ptr, shape, typestr), device=device)
+
+
+class Handle:
+    """One ns_handle: the device state of `batch` independent sequences."""
+
+    def __init__(self, V: int, H: int, W_max: int, K_pre: int = 3, K_ver: int = 3, max_tree: int = 64,
+                 max_k: int = 16, batch: int = 1, max_prompt: int = 4096):
+        self._lib = load_library()
+        self.cfg = ns_config(V, H, W_max, K_pre, K_ver, max_tree, max_k, batch, max_prompt)
+        self.device = torch.device("cuda", torch.cuda.current_device())
+        h = ctypes.c_void_p()
+        _check(self._lib.ns_create(ctypes.byref(self.cfg), ctypes.byref(h)), "ns_create")
+        self._h = h
+
+    # -- lifetime --------------------------------------------------------------
+    def close(self) -> None:
+        if self._h:
+            _check(self._lib.ns_destroy(self._h), "ns_destroy")
+            self._h = ctypes.c_void_p()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            if self._h:
+                self._lib.ns_destroy(self._h)
+        except Exception:
+            pass
+
+    @property
+    def device_bytes(self) -> int:
+        return int(self._lib.ns_device_bytes(self._h))
+
+    # -- the C ABI -------------------------------------------------------------
+    def stream_init(self, seq: int, prompt: torch.Tensor, prefill_logits: Optional[torch.Tensor],
+                    stream=None) -> None:
+        _check(self._lib.ns_stream_init(self._h, seq, _ptr(prompt, torch.int32, "prompt"), prompt.numel(),
+                                        _ptr(prefill_logits, torch.float32, "prefill_logits"), _stream(stream)),
+               "ns_stream_init")
+
+    def stream_append(self, seq: int, tree_ids: Optional[torch.Tensor], verify_logits: Optional[torch.Tensor],
+                      verify_row: int = 0, stream=None) -> None:
+        n_tree = 0 if tree_ids is None else tree_ids.numel()
+        n_v = 0 if verify_logits is None else (verify_logits.shape[0] if verify_logits.dim() == 2 else 1)
+        _check(self._lib.ns_stream_append(self._h, seq, _ptr(tree_ids, torch.int32, "tree_ids"), n_tree,
+                                          _ptr(verify_logits, torch.float32, "verify_logits"), n_v, verify_row,
+                                          _stream(stream)), "ns_stream_append")
+
+    def build_active_vocab(self, seq: int, stream=None) -> None:
+        _check(self._lib.ns_build_active_vocab(self._h, seq, _stream(stream)), "ns_build_active_vocab")
+
+    def gather_head_rows(self, seq: int, W_head: torch.Tensor, copy_stream=None,
+                         done: Optional[torch.cuda.Event] = None) -> None:
+        ev = done.cuda_event if done is not None else None
+        _check(self._lib.ns_gather_head_rows(self._h, seq, _ptr(W_head, _BF16, "W_head"), _stream(copy_stream), ev),
+               "ns_gather_head_rows")
+
+    def _outputs(self, n, k, ids, vals):
+        if ids is None:
+            ids = torch.empty((n, k), dtype=torch.int32, device=self.device)
+        if vals is None:
+            vals = torch.empty((n, k), dtype=torch.float32, device=self.device)
+        return ids, vals
+
+    def sub_lm_head_logits_topk(self, seq: int, hidden: torch.Tensor, k: int, logits: Optional[torch.Tensor] = None,
+                                ids: Optional[torch.Tensor] = None, vals: Optional[torch.Tensor] = None,
+                                stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        n = hidden.shape[0]
+        ids, vals = self._outputs(n, k, ids, vals)
+        ld = logits.shape[1] if logits is not None else 0
+        _check(self._lib.ns_sub_lm_head_logits_topk(self._h, seq, _ptr(hidden, _BF16, "hidden"), n, k,
+                                                    _ptr(logits, torch.float32, "logits"), ld,
+                                                    _ptr(ids, torch.int32, "ids"), _ptr(vals, torch.float32, "vals"),
+                                                    _stream(stream)), "ns_sub_lm_head_logits_topk")
+        return ids, vals
+
+    def step(self, seq: int, tree_ids: Optional[torch.Tensor], verify_logits: Optional[torch.Tensor],
+             verify_row: int, W_head: torch.Tensor, hidden: torch.Tensor, k: int,
+             logits: Optional[torch.Tensor] = None, ids: Optional[torch.Tensor] = None,
+             vals: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        n_tree = 0 if tree_ids is None else tree_ids.numel()
+        n_v = 0 if verify_logits is None else (verify_logits.shape[0] if verify_logits.dim() == 2 else 1)
+        n = hidden.shape[0]
+        ids, vals = self._outputs(n, k, ids, vals)
+        ld = logits.shape[1] if logits is not None else 0
+        _check(self._lib.ns_step(self._h, seq, _ptr(tree_ids, torch.int32, "tree_ids"), n_tree,
+                                 _ptr(verify_logits, torch.float32, "verify_logits"), n_v, verify_row,
+                                 _ptr(W_head, _BF16, "W_head"), _ptr(hidden, _BF16, "hidden"), n, k,
+                                 _ptr(logits, torch.float32, "logits"), ld, _ptr(ids, torch.int32, "ids"),
+                                 _ptr(vals, torch.float32, "vals"), _stream(stream)), "ns_step")
+        return ids, vals
+
+    def dense_lm_head_topk(self, W_head: torch.Tensor, rows: int, hidden: torch.Tensor, k: int,
+                           logits: Optional[torch.Tensor] = None, ids: Optional[torch.Tensor] = None,
+                           vals: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        n = hidden.shape[0]
+        ids, vals = self._outputs(n, k, ids, vals)
+        ld = logits.shape[1] if logits is not None else 0
+        _check(self._lib.ns_dense_lm_head_topk(self._h, _ptr(W_head, _BF16, "W_head"), rows,
+                                               _ptr(hidden, _BF16, "hidden"), n, k,
+                                               _ptr(logits, torch.float32, "logits"), ld,
+                                               _ptr(ids, torch.int32, "ids"), _ptr(vals, torch.float32, "vals"),
+                                               _stream(stream)), "ns_dense_lm_head_topk")
+        return ids, vals
+
+    # -- state views (device tensors aliasing library memory) ----------------
+    def get_active(self, seq: int):
+        """Views (ids int32 [W_max], count int32 [1], bitmap int32 [ceil(V/32)], packed int16 [W_max, H])."""
+        p = [ctypes.c_void_p() for _ in range(4)]
+        _check(self._lib.ns_get_active(self._h, seq, *[ctypes.byref(x) for x in p]), "ns_get_active")
+        c = self.cfg
+        nwords = (c.V + 31) // 32
+        return (_view(p[0].value, (c.W_max,), "<i4", self.device), _view(p[1].value, (1,), "<i4", self.device),
+                _view(p[2].value, (nwords,), "<i4", self.device),
+                _view(p[3].value, (c.W_max, c.H), "<i2", self.device))
+
+    def get_state(self, seq: int):
+        """Views (ring int32 [W_max], length int64 [1], counts int32 [V])."""
+        p = [ctypes.c_void_p() for _ in range(3)]
+        _check(self._lib.ns_get_state(self._h, seq, *[ctypes.byref(x) for x in p]), "ns_get_state")
+        c = self.cfg
+        return (_view(p[0].value, (c.W_max,), "<i4", self.device), _view(p[1].value, (1,), "<i8", self.device),
+                _view(p[2].value, (c.V,), "<i4", self.device))
+
+    def get_error(self, clear: bool = False) -> int:
+        f = ctypes.c_uint32()
+        _check(self._lib.ns_get_error(self._h, ctypes.byref(f), int(clear)), "ns_get_error")
+        return int(f.value)

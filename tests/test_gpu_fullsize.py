@@ -1,0 +1,130 @@
+"""GPU parity at the full workload sizes, through the fused step the benchmark times.
+
+State (I_t, count, bitmap, |S|) is compared with the oracle on every decode
+step.  Ring, window counts, the packed sub-head, logits and top-k are compared
+on sampled steps (the first four, every 16th and the last).  The dense heads
+are checked on sampled columns plus the top-k's consistency with the logits.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import Workload, get_config
+
+from parity import LOGIT_RTOL, check_logits, check_packed, check_projection, check_state, dev_bf16, dev_f32, dev_i32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import speculative_decoding_draft_stream_gb300 as p
+    from speculative_decoding_draft_stream_gb300 import build
+
+    build.build()
+    p.load_library()
+    return p
+
+
+def _sampled(steps):
+    return set(range(min(4, steps))) | set(range(0, steps, 16)) | {steps - 1}
+
+
+def _run(pkg, cfg, wl, W, W_dev, h, seq, max_steps=None):
+    steps = cfg.steps if max_steps is None else min(cfg.steps, max_steps)
+    sample = _sampled(steps)
+    prompt = wl.prompt(seq)
+    Z = wl.prefill_logits(seq)
+    ost = oracle.OracleStream(cfg.V, cfg.W_max, cfg.K_pre, cfg.K_ver)
+    ost.init(prompt, Z)
+    h.stream_init(seq, dev_i32(prompt), dev_f32(Z))
+    del Z
+    h.build_active_vocab(seq)
+    check_state(h, seq, ost, full=True)
+    trees = wl.trees(seq)
+    logits = torch.zeros((cfg.n_tree, cfg.W_max), dtype=torch.float32, device="cuda")
+    sizes = []
+    for t in range(steps):
+        vb, vr, hid = wl.verify_logits(seq, t), wl.verify_row(seq, t), wl.hiddens(seq, t)
+        ids, vals = h.step(seq, dev_i32(trees[t]), dev_f32(vb), vr, W_dev, dev_bf16(hid), cfg.k, logits=logits)
+        ost.append(trees[t], vb, vr)
+        I = check_state(h, seq, ost, full=t in sample)
+        sizes.append(len(I))
+        if t in sample:
+            check_packed(h, seq, W, I)
+            check_projection(logits, ids, vals, hid, W, I, cfg.k)
+    return sizes
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_v128256_h4096", "qwen25_7b_v152064_h3584"])
+def test_full_config(pkg, name):
+    cfg = get_config(name)
+    wl = Workload(cfg)
+    W = wl.w_head()
+    W_dev = dev_bf16(W)
+    with pkg.Handle(cfg.V, cfg.H, cfg.W_max, cfg.K_pre, cfg.K_ver, max_tree=cfg.n_tree, max_k=cfg.k,
+                    max_prompt=cfg.prompt_len) as h:
+        sizes = _run(pkg, cfg, wl, W, W_dev, h, 0)
+        assert h.get_error() == 0
+    assert max(sizes) <= cfg.W_max and min(sizes) > 0
+
+
+def _check_dense(h, W, W_dev, hid, rows, k, rng):
+    logits = torch.zeros((hid.shape[0], rows), dtype=torch.float32, device="cuda")
+    ids, vals = h.dense_lm_head_topk(W_dev, rows, dev_bf16(hid), k, logits=logits)
+    ids, vals = ids.cpu().numpy(), vals.cpu().numpy()
+    cols = np.unique(np.concatenate([rng.choice(rows, size=2048, replace=False), ids.ravel()]))
+    want = oracle.project(hid, W[cols])
+    got = logits[:, torch.from_numpy(cols).cuda()].cpu().numpy()
+    # tolerance scale: the largest |logit| over the sampled columns (a lower
+    # bound of the row maximum, so the bound is at least as strict)
+    tol = check_logits(got, want)
+    pos = {int(c): j for j, c in enumerate(cols.tolist())}
+    full = logits.cpu().numpy()
+    for r in range(hid.shape[0]):
+        assert len(set(ids[r].tolist())) == k
+        for p in range(k):
+            assert abs(vals[r, p] - want[r, pos[int(ids[r, p])]]) <= tol[r]
+            assert vals[r, p] == full[r, ids[r, p]]
+        # the top-k is the top-k of the logits the kernel wrote (ties to the smaller id)
+        order = sorted(range(rows), key=lambda j: (-float(full[r, j]), j))[:k] if rows <= 4096 else None
+        if order is not None:
+            assert ids[r].tolist() == order
+        else:
+            kth = np.partition(full[r], rows - k)[rows - k]
+            assert vals[r, -1] == kth and (full[r] > vals[r, 0]).sum() == 0
+
+
+@pytest.mark.parametrize("W_max", [512, 1024, 2048, 3072, 4096, 8192])
+def test_qwen3_sweep(pkg, W_max):
+    base = get_config("qwen3_8b_v151936_h4096")
+    cfg = base.with_(W_max=W_max)
+    wl = Workload(cfg)
+    W = wl.w_head()
+    W_dev = dev_bf16(W)
+    rng = np.random.default_rng(W_max)
+    with pkg.Handle(cfg.V, cfg.H, cfg.W_max, cfg.K_pre, cfg.K_ver, max_tree=cfg.n_tree, max_k=cfg.k,
+                    max_prompt=cfg.prompt_len) as h:
+        _run(pkg, cfg, wl, W, W_dev, h, 0)
+        assert h.get_error() == 0
+        if W_max == 3072:
+            for t in (0, cfg.steps - 1):
+                hid = wl.hiddens(0, t)
+                _check_dense(h, W, W_dev, hid, cfg.V, cfg.k, rng)      # full-vocabulary head
+                _check_dense(h, W, W_dev, hid, 32768, cfg.k, rng)      # static first-32768-ids sub-head
+
+
+def test_batched_sequences(pkg):
+    cfg = get_config("batched16_v128256_h4096")
+    wl = Workload(cfg)
+    W = wl.w_head()
+    W_dev = dev_bf16(W)
+    with pkg.Handle(cfg.V, cfg.H, cfg.W_max, cfg.K_pre, cfg.K_ver, max_tree=cfg.n_tree, max_k=cfg.k,
+                    batch=cfg.batch, max_prompt=cfg.prompt_len_max) as h:
+        for b in range(cfg.batch):
+            _run(pkg, cfg, wl, W, W_dev, h, b)
+        assert h.get_error() == 0
