@@ -1,0 +1,487 @@
+#!/usr/bin/env python
+"""Benchmark of the per-step dynamic-vocabulary draft LM head on GB300.
+
+One step = one decode step of the hot path on one sequence: verify Top-K,
+draft-tree dedup, stream append, window counts and bitmap, ascending
+compaction into I_t, gather of W_head[I_t, :] into the packed buffer,
+projection of the draft hidden states and top-k remapped to global ids
+(ns_step: three kernels).  Workload: Llama-3-8B-shaped draft head (V=128256,
+H=4096, W_max=3072, K_pre=K_ver=3, 60-node trees, top-10), seeded synthetic
+inputs resident in HBM before the timed region.  L2 (129 MB) is flushed
+between timed steps by writing a 256 MiB buffer, outside the timed events:
+between two draft steps a real system runs the target model, which evicts
+the sub-head rows.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on
+the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft sub-LM-head steps/sec and us/step at V=128k,H=4096,|I_t|~3k; % HBM roofline"
+DEFAULT_WORKLOAD = "llama3_8b_v128256_h4096"
+FLUSH_BYTES = 256 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gather_project_traffic.json")
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=512)
+    p.add_argument("--warmup", type=int, default=8)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-extra", action="store_true", help="skip the dense-head and pinned-point extras")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            sel = [f"--id={self.index}"] if self.index is not None else []
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        load = [r for r in rows if (num(r[4]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in load if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i in range(4) if r[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(load)}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("ns_project.cu", "ns_internal.cuh"):
+        with open(os.path.join(ROOT, "speculative_decoding_draft_stream_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic_per_byte():
+    """DRAM bytes per algorithmic byte of the fused gather+projection kernel,
+    from the committed ncu summary, if it was taken on the current source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    if d.get("source_hash") != source_hash():
+        return None
+    return float(d["dram_bytes"]) / float(d["algorithmic_bytes"])
+
+
+def step_bytes(m, n, H, V):
+    """Algorithmic bytes of one whole step: rows read + packed written,
+    logits written, hiddens read, one verify row read, bitmap and I_t."""
+    return 2 * m * H * 2 + n * m * 4 + n * H * 2 + V * 4 + 2 * ((V + 7) // 8) + 4 * m
+
+
+def proj_bytes(m, n, H):
+    """Algorithmic bytes of the fused gather + projection kernel."""
+    return 2 * m * H * 2 + n * m * 4 + n * H * 2 + 4 * m
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+def time_oracle(cfg, wl, steps_wanted: int, budget_s: float, warmup: int = 0):
+    import oracle
+
+    W = wl.w_head()
+    ost = oracle.OracleStream(cfg.V, cfg.W_max, cfg.K_pre, cfg.K_ver)
+    ost.init(wl.prompt(0), wl.prefill_logits(0))
+    trees = wl.trees(0)
+
+    def one(t):
+        u = t % cfg.steps
+        ost.append(trees[u], wl.verify_logits(0, u), wl.verify_row(0, u))
+        I = ost.active()
+        oracle.sub_head_step(wl.hiddens(0, u), W, I, cfg.k)
+
+    for t in range(warmup):
+        one(t)
+    done = 0
+    t0 = time.perf_counter()
+    while done < steps_wanted:
+        one(warmup + done)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done, dt
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from synth import Workload, get_config
+
+    cfg = get_config(args.workload)
+    wl = Workload(cfg)
+    done, dt = time_oracle(cfg, wl, args.steps, budget_s=150.0, warmup=args.warmup)
+    v = done / dt
+    cores = oracle_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * dt / done, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "V": cfg.V, "H": cfg.H, "W_max": cfg.W_max, "n_tree": cfg.n_tree,
+                   "k": cfg.k},
+        "cpu_baseline": {"value": v, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {done} decode steps of {cfg.name} after its prefill init"},
+        "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our CUDA path
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from speculative_decoding_draft_stream_gb300 import build as nsbuild
+
+    nsbuild.build()
+    import speculative_decoding_draft_stream_gb300 as ns
+    from synth import Workload, get_config
+
+    cfg = get_config(args.workload)
+    wl = Workload(cfg)
+    seq = rank  # replicas: every rank decodes its own sequence
+    n, H, V, k = cfg.n_tree, cfg.H, cfg.V, cfg.k
+    T = cfg.steps
+
+    # ---- inputs, resident in HBM -------------------------------------------
+    W = wl.w_head()
+    W_d = torch.from_numpy(W.view(np.int16)).to(dev)
+    prompt = wl.prompt(seq)
+    prompt_d = torch.from_numpy(prompt).to(dev)
+    Z_d = torch.from_numpy(wl.prefill_logits(seq)).to(dev)
+    trees_h = wl.trees(seq)
+    trees_d = torch.from_numpy(trees_h).to(dev)
+    verify_h = np.stack([wl.verify_logits(seq, t) for t in range(T)])  # [T, n_v, V]
+    vrows = [wl.verify_row(seq, t) for t in range(T)]
+    hid_h = np.stack([wl.hiddens(seq, t) for t in range(T)]).view(np.int16)  # [T, n, H]
+    verify_d = torch.from_numpy(verify_h).to(dev)
+    hid_d = torch.from_numpy(hid_h).to(dev)
+    logits = torch.empty((n, cfg.W_max), dtype=torch.float32, device=dev)
+    ids = torch.empty((n, k), dtype=torch.int32, device=dev)
+    vals = torch.empty((n, k), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    h = ns.Handle(V, H, cfg.W_max, cfg.K_pre, cfg.K_ver, max_tree=n, max_k=k, max_prompt=len(prompt))
+    stream = torch.cuda.current_stream()
+
+    def init():
+        h.stream_init(0, prompt_d, Z_d)
+        h.build_active_vocab(0)
+
+    def step(t):
+        u = t % T
+        h.step(0, trees_d[u], verify_d[u], vrows[u], W_d, hid_d[u], k, logits=logits, ids=ids, vals=vals)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    clocks = ClockSampler(local if world > 1 else None)
+    clocks.start()
+
+    # ---- prefill init (per request, timed on its own) ------------------------
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    init()  # first call pays one-time costs
+    torch.cuda.synchronize()
+    flush.zero_()
+    e0.record()
+    init()
+    e1.record()
+    torch.cuda.synchronize()
+    init_ms = e0.elapsed_time(e1)
+
+    # ---- warm-up, then the timed decode steps -------------------------------
+    # The K steps (each preceded by an L2 flush) are captured into one CUDA
+    # graph and replayed once, so the host never paces the GPU.  ns_step
+    # records four events per step (external graph nodes): before its first
+    # kernel, after the state update, after the fused gather + projection,
+    # after the top-k.  A step's time is first to last event; flushes fall
+    # outside.
+    for t in range(args.warmup):
+        step(t)
+    K = args.steps
+    tev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for evs in tev:
+        for e in evs:
+            e.record()  # torch creates CUDA events lazily; create them before capture
+    act, cnt, _, _ = h.get_active(0)
+    counts = torch.zeros(K, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for t in range(K):
+            flush.zero_()
+            h.trace_events(tev[t])
+            step(t)
+            counts[t:t + 1].copy_(cnt)
+        h.trace_events(None)
+    init()
+    barrier()
+    graph.replay()
+    barrier()
+    if h.get_error() != 0:
+        raise RuntimeError("device error flags set during the timed steps")
+    per_step_ms = [a[0].elapsed_time(a[3]) for a in tev]
+    total_ms = max_over_ranks(sum(per_step_ms))
+    steps_per_s = world * K / (total_ms / 1e3)
+    ms_state = [a[0].elapsed_time(a[1]) for a in tev]
+    ms_proj = [a[1].elapsed_time(a[2]) for a in tev]
+    ms_topk = [a[2].elapsed_time(a[3]) for a in tev]
+    m_list = counts.cpu().tolist()
+    del graph
+    pb = sum(proj_bytes(m, n, H) for m in m_list)
+    proj_gbs = pb / (sum(ms_proj) * 1e-3) / 1e9
+    sb = sum(step_bytes(m, n, H, V) for m in m_list)
+    step_gbs = sb / (sum(per_step_ms) * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+    ratio = ncu_traffic_per_byte()
+
+    # ---- end to end through the public API with host buffers -----------------
+    init()
+    trees_p = torch.from_numpy(trees_h).pin_memory()
+    verify_p = torch.from_numpy(verify_h).pin_memory()
+    hid_p = torch.from_numpy(hid_h).pin_memory()
+    tree_b = torch.empty((n,), dtype=torch.int32, device=dev)
+    ver_b = torch.empty(verify_h.shape[1:], dtype=torch.float32, device=dev)
+    hid_b = torch.empty((n, H), dtype=torch.int16, device=dev)
+    ids_p = torch.empty((n, k), dtype=torch.int32, pin_memory=True)
+    vals_p = torch.empty((n, k), dtype=torch.float32, pin_memory=True)
+    h2d = trees_p[0].numel() * 4 + verify_p[0].numel() * 4 + hid_p[0].numel() * 2
+    d2h = ids_p.numel() * 4 + vals_p.numel() * 4
+    barrier()
+    e2e_s = 0.0
+    for t in range(K):
+        u = t % T
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        tree_b.copy_(trees_p[u], non_blocking=True)
+        ver_b.copy_(verify_p[u], non_blocking=True)
+        hid_b.copy_(hid_p[u], non_blocking=True)
+        h.step(0, tree_b, ver_b, vrows[u], W_d, hid_b, k, logits=logits, ids=ids, vals=vals)
+        ids_p.copy_(ids, non_blocking=True)
+        vals_p.copy_(vals, non_blocking=True)
+        stream.synchronize()
+        e2e_s += time.perf_counter() - t0
+    barrier()
+    e2e_s = max_over_ranks(e2e_s)
+    e2e = world * K / e2e_s
+
+    # ---- extras: the |I_t|~3k point and the dense heads ----------------------
+    # Each is timed as (graph of R x [flush + op]) - (graph of R x [flush]).
+    extra = {}
+    if not args.no_extra:
+        def graph_us(fn, reps=32):
+            def capture(with_op):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for _ in range(reps):
+                        flush.zero_()
+                        if with_op:
+                            fn()
+                return g
+
+            fn()
+            torch.cuda.synchronize()
+            g_op, g_fl = capture(True), capture(False)
+            out = []
+            for g in (g_op, g_fl, g_op, g_fl):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                torch.cuda.synchronize()
+                out.append(a.elapsed_time(b))
+            return 1e3 * min(out[0] - out[1], out[2] - out[3]) / reps
+
+        init()
+        torch.cuda.synchronize()
+        m0 = int(cnt.item())
+        # the sub-head step on the post-prefill window (|I_t| ~ W_max): build,
+        # gather + projection + top-k; nothing is appended, so it repeats
+        us0 = graph_us(lambda: (h.build_active_vocab(0),
+                                h.gather_sub_lm_head_topk(0, W_d, hid_d[0], k, logits=logits, ids=ids, vals=vals)))
+        b0 = step_bytes(m0, n, H, V) - V * 4  # no verify row in this sub-head step
+        extra["pinned_point"] = {"active": m0, "us": us0, "frac_of_peak": b0 / (us0 * 1e-6) / 1e9 / peak}
+
+        hid_bf = hid_d[0].view(torch.bfloat16)
+        W_bf = W_d.view(torch.bfloat16)
+        dense_out = torch.empty((n, V), dtype=torch.bfloat16, device=dev)
+        dense_logits = torch.empty((n, V), dtype=torch.float32, device=dev)
+        us_cublas = graph_us(lambda: torch.matmul(hid_bf, W_bf.t(), out=dense_out))
+        us_dense = graph_us(lambda: h.dense_lm_head_topk(W_d, V, hid_d[0], k, logits=dense_logits, ids=ids,
+                                                         vals=vals))
+        us_static = graph_us(lambda: h.dense_lm_head_topk(W_d, 32768, hid_d[0], k, logits=dense_logits, ids=ids,
+                                                          vals=vals))
+        extra["dense_head"] = {"cublas_matmul_us": us_cublas, "ours_dense_topk_us": us_dense,
+                               "ours_static32768_topk_us": us_static,
+                               "speedup_step_vs_cublas_dense": us_cublas / (1e3 * total_ms / K),
+                               "speedup_pinned_point_vs_cublas_dense": us_cublas / us0}
+    clock = clocks.stop()
+
+    # ---- the CPU oracle on a bounded sample (rank 0, one GPU) ----------------
+    cpu = None
+    if rank == 0 and world == 1:
+        done, dt = time_oracle(cfg, wl, T, budget_s=args.cpu_seconds)
+        cpu = {"value": done / dt, "unit": "steps/s", "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"first {done} decode steps of {cfg.name} after its prefill init (prefill not timed)"}
+
+    if rank == 0:
+        mean_m = float(np.mean(m_list))
+        line = {
+            "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": total_ms / K, "us_per_step": 1e3 * total_ms / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": cfg.name, "V": V, "H": H, "W_max": cfg.W_max, "K_pre": cfg.K_pre,
+                       "K_ver": cfg.K_ver, "n_tree": n, "k": k, "decode_steps_per_pass": T,
+                       "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+                       "mean_active": mean_m, "min_active": int(min(m_list)), "max_active": int(max(m_list)),
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "project_kernel<gather> (fused gather + projection)",
+                         "achieved": proj_gbs, "peak": peak, "unit": "GB/s", "frac": proj_gbs / peak,
+                         "peak_kind": f"{peak_kind} hbm_gbs",
+                         "traffic": (ratio * pb / K) if ratio is not None else None,
+                         "algorithmic_bytes_per_launch": pb / K},
+            "step_roofline": {"achieved": step_gbs, "frac": step_gbs / peak,
+                              "bytes_per_step": sb / K},
+            "kernel_us": {"state_update": 1e3 * float(np.mean(ms_state)),
+                          "gather_project": 1e3 * float(np.mean(ms_proj)),
+                          "topk": 1e3 * float(np.mean(ms_topk))},
+            "init_ms": init_ms,
+            "e2e": {"value": e2e, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * K,
+            "clocks": clock,
+            "cpu_baseline": cpu,
+            "extra": extra,
+        }
+        print(json.dumps(line), flush=True)
+    h.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

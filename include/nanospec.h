@@ -188,6 +188,38 @@ NS_API ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, i
                   ns_stream stream);
 
 /*
+ * The state half of ns_step in one launch: ns_stream_append followed by
+ * ns_build_active_vocab (the "GPU-resident state update" that determines
+ * I_{t+1}, MicroSpec §3.3).  Arguments as ns_stream_append.
+ */
+NS_API ns_status ns_state_update(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
+                                 const float *d_verify_logits, int32_t n_verify, int32_t verify_row,
+                                 ns_stream stream);
+
+/*
+ * The sub-head half of ns_step: the gather of W_head[I_t, :] into the packed
+ * buffer fused with the projection (each row is read from HBM once, written
+ * to the packed buffer and multiplied while on chip), then the top-k.
+ * Results as ns_gather_head_rows followed by ns_sub_lm_head_logits_topk.
+ */
+NS_API ns_status ns_gather_sub_lm_head_topk(ns_handle *h, int32_t seq, const uint16_t *d_W_head,
+                                            const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
+                                            int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
+                                            ns_stream stream);
+
+/*
+ * Per-kernel event trace (MicroSpec §4 profiles per-step latency with CUDA
+ * event recording).  While set, ns_step records, on its stream,
+ *   events[0] before its first kernel,
+ *   events[1] after the state update (append + active vocabulary),
+ *   events[2] after the fused gather + projection,
+ *   events[3] after the top-k.
+ * events must stay valid while set; n_events must be 4, or 0 with
+ * events == NULL to switch tracing off.  The events are borrowed cudaEvent_t.
+ */
+NS_API ns_status ns_trace_events(ns_handle *h, ns_event *events, int32_t n_events);
+
+/*
  * Dense head on a fixed row range: logits over rows [0, rows) of W_head
  * (rows = V is the full-vocabulary LM head of Eq. 1; rows = 32768 a static
  * frequency-ranked sub-head) and per-row top-k with ids = row numbers.

@@ -29,6 +29,8 @@ struct ns_handle {
   float *dense_part = nullptr;    // [pgrid x tile]
   int32_t *dense_tickets = nullptr;
   int dense_ld = 0;
+  cudaEvent_t trace[4] = {nullptr, nullptr, nullptr, nullptr};
+  bool tracing = false;
 };
 
 namespace {
@@ -243,20 +245,32 @@ ns_status ns_sub_lm_head_logits_topk(ns_handle *h, int32_t seq, const uint16_t *
   return cuda_status(e);
 }
 
-ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
-                  const float *d_verify_logits, int32_t n_verify, int32_t verify_row, const uint16_t *d_W_head,
-                  const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits, int32_t ld_logits,
-                  int32_t *d_topk_ids, float *d_topk_vals, ns_stream stream) {
+ns_status ns_state_update(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
+                          const float *d_verify_logits, int32_t n_verify, int32_t verify_row, ns_stream stream) {
   ns_status st = check_append_args(h, seq, d_tree_ids, n_tree, d_verify_logits, n_verify, verify_row);
   if (st != NS_OK) return st;
-  if (!d_W_head || !aligned16(d_W_head)) return NS_ERR_ARG;
-  st = check_proj_args(h, d_hidden, n, k, d_logits, ld_logits, h->cfg.W_max, d_topk_ids, d_topk_vals);
-  if (st != NS_OK) return st;
-  const ns::SeqDev &s = h->seqs[seq];
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
-  cudaError_t e = ns::launch_append(s, h->dims, h->vgrid, d_tree_ids, n_tree, zrow, true, h->err, cs);
-  if (e != cudaSuccess) return NS_ERR_CUDA;
+  return cuda_status(ns::launch_append(h->seqs[seq], h->dims, h->vgrid, d_tree_ids, n_tree, zrow, true, h->err,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+static ns_status check_gather_project_args(ns_handle *h, int32_t seq, const uint16_t *d_W_head,
+                                           const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
+                                           int32_t ld_logits, int32_t *d_ids, float *d_vals) {
+  if (!valid_seq(h, seq) || !d_W_head || !aligned16(d_W_head)) return NS_ERR_ARG;
+  ns_status st = check_proj_args(h, d_hidden, n, k, d_logits, ld_logits, h->cfg.W_max, d_ids, d_vals);
+  if (st != NS_OK) return st;
+  if (!h->inited[seq]) return NS_ERR_STATE;
+  return NS_OK;
+}
+
+// Fused gather + projection, then top-k; `mid` (nullable) is recorded
+// between the two kernels.
+static cudaError_t enqueue_gather_project(ns_handle *h, int32_t seq, const uint16_t *d_W_head,
+                                          const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
+                                          int32_t ld_logits, int32_t *d_ids, float *d_vals, cudaStream_t cs,
+                                          cudaEvent_t mid) {
+  const ns::SeqDev &s = h->seqs[seq];
   ns::ProjArgs a{};
   a.rows = d_W_head;
   a.idx = s.active;
@@ -269,9 +283,62 @@ ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t 
   a.ld = d_logits ? ld_logits : h->dims.ld_scratch;
   a.part = s.ppart;
   a.tickets = s.pticket;
-  e = ns::launch_project(ns::kGatherRows, a, h->pgrid, cs);
-  if (e == cudaSuccess) e = ns::launch_topk(a.logits, a.ld, s.count, 0, s.active, n, k, d_topk_ids, d_topk_vals, cs);
+  cudaError_t e = ns::launch_project(ns::kGatherRows, a, h->pgrid, cs);
+  if (e == cudaSuccess && mid) e = cudaEventRecordWithFlags(mid, cs, cudaEventRecordExternal);
+  if (e == cudaSuccess) e = ns::launch_topk(a.logits, a.ld, s.count, 0, s.active, n, k, d_ids, d_vals, cs);
+  return e;
+}
+
+ns_status ns_gather_sub_lm_head_topk(ns_handle *h, int32_t seq, const uint16_t *d_W_head, const uint16_t *d_hidden,
+                                     int32_t n, int32_t k, float *d_logits, int32_t ld_logits, int32_t *d_topk_ids,
+                                     float *d_topk_vals, ns_stream stream) {
+  ns_status st = check_gather_project_args(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids,
+                                           d_topk_vals);
+  if (st != NS_OK) return st;
+  return cuda_status(enqueue_gather_project(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids,
+                                            d_topk_vals, static_cast<cudaStream_t>(stream), nullptr));
+}
+
+// Trace events are recorded as external event nodes when the stream is being
+// captured into a CUDA graph, so a captured step still times its kernels.
+static cudaError_t trace_record(cudaEvent_t ev, cudaStream_t st) {
+  return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+}
+
+ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
+                  const float *d_verify_logits, int32_t n_verify, int32_t verify_row, const uint16_t *d_W_head,
+                  const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits, int32_t ld_logits,
+                  int32_t *d_topk_ids, float *d_topk_vals, ns_stream stream) {
+  ns_status st = check_append_args(h, seq, d_tree_ids, n_tree, d_verify_logits, n_verify, verify_row);
+  if (st != NS_OK) return st;
+  st = check_gather_project_args(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals);
+  if (st != NS_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const bool tr = h->tracing;
+  cudaError_t e = tr ? trace_record(h->trace[0], cs) : cudaSuccess;
+  const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
+  if (e == cudaSuccess) e = ns::launch_append(h->seqs[seq], h->dims, h->vgrid, d_tree_ids, n_tree, zrow, true, h->err, cs);
+  if (e == cudaSuccess && tr) e = trace_record(h->trace[1], cs);
+  if (e == cudaSuccess)
+    e = enqueue_gather_project(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals, cs,
+                               tr ? h->trace[2] : nullptr);
+  if (e == cudaSuccess && tr) e = trace_record(h->trace[3], cs);
   return cuda_status(e);
+}
+
+ns_status ns_trace_events(ns_handle *h, ns_event *events, int32_t n_events) {
+  if (!h) return NS_ERR_ARG;
+  if (n_events == 0 && !events) {
+    h->tracing = false;
+    return NS_OK;
+  }
+  if (!events || n_events != 4) return NS_ERR_ARG;
+  for (int i = 0; i < 4; ++i) {
+    if (!events[i]) return NS_ERR_ARG;
+    h->trace[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  h->tracing = true;
+  return NS_OK;
 }
 
 ns_status ns_dense_lm_head_topk(ns_handle *h, const uint16_t *d_W_head, int32_t rows, const uint16_t *d_hidden,

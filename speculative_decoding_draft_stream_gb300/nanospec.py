@@ -31,7 +31,8 @@ MAX_ROWS = 64
 EXPORTED = (
     "ns_status_string", "ns_create", "ns_destroy", "ns_device_bytes", "ns_stream_init", "ns_stream_append",
     "ns_build_active_vocab", "ns_gather_head_rows", "ns_sub_lm_head_logits_topk", "ns_step",
-    "ns_dense_lm_head_topk", "ns_get_active", "ns_get_state", "ns_get_error",
+    "ns_dense_lm_head_topk", "ns_get_active", "ns_get_state", "ns_get_error", "ns_state_update",
+    "ns_gather_sub_lm_head_topk", "ns_trace_events",
 )
 
 
@@ -74,6 +75,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                 ctypes.POINTER(P)]),
         "ns_get_state": (I32, [P, I32, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P)]),
         "ns_get_error": (I32, [P, ctypes.POINTER(ctypes.c_uint32), I32]),
+        "ns_state_update": (I32, [P, I32, P, I32, P, I32, I32, P]),
+        "ns_gather_sub_lm_head_topk": (I32, [P, I32, U16P, U16P, I32, I32, P, I32, P, P, P]),
+        "ns_trace_events": (I32, [P, ctypes.POINTER(P), I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -214,6 +218,41 @@ class Handle:
                                  _ptr(logits, torch.float32, "logits"), ld, _ptr(ids, torch.int32, "ids"),
                                  _ptr(vals, torch.float32, "vals"), _stream(stream)), "ns_step")
         return ids, vals
+
+    def state_update(self, seq: int, tree_ids: Optional[torch.Tensor], verify_logits: Optional[torch.Tensor],
+                     verify_row: int = 0, stream=None) -> None:
+        n_tree = 0 if tree_ids is None else tree_ids.numel()
+        n_v = 0 if verify_logits is None else (verify_logits.shape[0] if verify_logits.dim() == 2 else 1)
+        _check(self._lib.ns_state_update(self._h, seq, _ptr(tree_ids, torch.int32, "tree_ids"), n_tree,
+                                         _ptr(verify_logits, torch.float32, "verify_logits"), n_v, verify_row,
+                                         _stream(stream)), "ns_state_update")
+
+    def gather_sub_lm_head_topk(self, seq: int, W_head: torch.Tensor, hidden: torch.Tensor, k: int,
+                                logits: Optional[torch.Tensor] = None, ids: Optional[torch.Tensor] = None,
+                                vals: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        n = hidden.shape[0]
+        ids, vals = self._outputs(n, k, ids, vals)
+        ld = logits.shape[1] if logits is not None else 0
+        _check(self._lib.ns_gather_sub_lm_head_topk(self._h, seq, _ptr(W_head, _BF16, "W_head"),
+                                                    _ptr(hidden, _BF16, "hidden"), n, k,
+                                                    _ptr(logits, torch.float32, "logits"), ld,
+                                                    _ptr(ids, torch.int32, "ids"), _ptr(vals, torch.float32, "vals"),
+                                                    _stream(stream)), "ns_gather_sub_lm_head_topk")
+        return ids, vals
+
+    def trace_events(self, events) -> None:
+        """Record ns_step's kernel boundaries on four torch.cuda.Events (None: off)."""
+        if events is None:
+            _check(self._lib.ns_trace_events(self._h, None, 0), "ns_trace_events")
+            self._trace = None
+            return
+        events = list(events)
+        for e in events:
+            if not e.cuda_event:  # torch creates the CUDA event on its first record
+                e.record()
+        arr = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+        _check(self._lib.ns_trace_events(self._h, arr, 4), "ns_trace_events")
+        self._trace = (arr, list(events))  # keep the events alive while set
 
     def dense_lm_head_topk(self, W_head: torch.Tensor, rows: int, hidden: torch.Tensor, k: int,
                            logits: Optional[torch.Tensor] = None, ids: Optional[torch.Tensor] = None,

@@ -29,6 +29,7 @@ Token ids are 0-based (the papers number the vocabulary ``1..V``).
 from __future__ import annotations
 
 import dataclasses
+import os
 from dataclasses import dataclass
 from functools import lru_cache
 from typing import Optional
@@ -197,9 +198,26 @@ class Workload:
         return out
 
     def w_head(self) -> np.ndarray:
-        """The whole LM head W_head [V, H] (bf16 bits), generated once."""
+        """The whole LM head W_head [V, H] (bf16 bits), generated once.
+
+        Row chunks are independent streams, so they are drawn in parallel
+        threads (numpy releases the GIL); the bytes do not depend on the
+        thread count."""
         if self._w is None:
-            self._w = self.w_head_rows(0, self.cfg.V)
+            from concurrent.futures import ThreadPoolExecutor
+
+            c = self.cfg
+            out = np.empty((c.V, c.H), dtype=np.uint16)
+            span = 16 * W_ROW_CHUNK
+
+            def fill(r0):
+                r1 = min(r0 + span, c.V)
+                out[r0:r1] = self.w_head_rows(r0, r1)
+
+            workers = max(1, min(16, os.cpu_count() or 1))
+            with ThreadPoolExecutor(max_workers=workers) as ex:
+                list(ex.map(fill, range(0, c.V, span)))
+            self._w = out
         return self._w
 
     # -- prompt and prefill --------------------------------------------------

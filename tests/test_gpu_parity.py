@@ -304,3 +304,30 @@ def test_dense_head_mid(pkg):
         tol = check_logits(logits.cpu().numpy(), want)
         check_topk(ids.cpu().numpy(), vals.cpu().numpy(), want, np.arange(cfg.V), cfg.k, tol)
         assert torch.equal(ids, ids2) and torch.equal(vals, vals2)
+
+
+def test_trace_events_bracket_the_step(pkg):
+    """ns_trace_events records the step's kernel boundaries and leaves results unchanged."""
+    cfg = TOY.with_(steps=3)
+    wl = Workload(cfg)
+    W = wl.w_head()
+    W_dev = dev_bf16(W)
+    with _handle(pkg, cfg, max_prompt=256) as h:
+        p, Z = wl.prompt(0), wl.prefill_logits(0)
+        o = oracle.OracleStream(cfg.V, cfg.W_max, cfg.K_pre, cfg.K_ver)
+        o.init(p, Z)
+        h.stream_init(0, dev_i32(p), dev_f32(Z))
+        logits = torch.zeros((cfg.n_tree, cfg.W_max), dtype=torch.float32, device="cuda")
+        for t in range(cfg.steps):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]  # not yet created by torch
+            h.trace_events(evs)
+            tr, vb, vr, hid = wl.trees(0)[t], wl.verify_logits(0, t), wl.verify_row(0, t), wl.hiddens(0, t)
+            ids, vals = h.step(0, dev_i32(tr), dev_f32(vb), vr, W_dev, dev_bf16(hid), cfg.k, logits=logits)
+            h.trace_events(None)
+            torch.cuda.synchronize()
+            spans = [evs[i].elapsed_time(evs[i + 1]) for i in range(3)]
+            assert all(s >= 0 for s in spans) and sum(spans) > 0
+            o.append(tr, vb, vr)
+            I = check_state(h, 0, o)
+            check_projection(logits, ids, vals, hid, W, I, cfg.k)
+        assert h._lib.ns_trace_events(h._h, None, 3) == -1  # wrong event count
