@@ -52,6 +52,9 @@ def parse_args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-extra", action="store_true", help="skip the dense-head and pinned-point extras")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
+    p.add_argument("--decode-steps", type=int, default=0,
+                   help="generate inputs for only this many decode steps (0: the workload's count); "
+                        "timed steps cycle through them")
     return p.parse_args()
 
 
@@ -247,7 +250,7 @@ def run_ours(args):
     wl = Workload(cfg)
     seq = rank  # replicas: every rank decodes its own sequence
     n, H, V, k = cfg.n_tree, cfg.H, cfg.V, cfg.k
-    T = cfg.steps
+    T = min(cfg.steps, args.decode_steps) if args.decode_steps > 0 else cfg.steps
 
     # ---- inputs, resident in HBM -------------------------------------------
     W = wl.w_head()

@@ -233,6 +233,33 @@ NS_API ns_status ns_dense_lm_head_topk(ns_handle *h, const uint16_t *d_W_head, i
                                 ns_stream stream);
 
 /*
+ * Dense head without any allocation (the paper has no counterpart: this is a
+ * service for callers that cannot allocate device memory — code that lives
+ * inside another framework's memory pool or a fixed memory budget, or a
+ * plugin that is only handed pointers — and therefore cannot hold a handle,
+ * because ns_create allocates).
+ * Same arguments and results as ns_dense_lm_head_topk, with H given directly
+ * instead of through a handle: logits over rows [0, rows) of W_head (bf16
+ * [rows x H], 64 <= H <= 8192, H % 64 == 0) and per-row top-k with ids = row
+ * numbers.  It calls no cudaMalloc/cudaFree and no allocating library
+ * routine.  Its scratch is a fixed array of about 6.6 MB inside the library
+ * image, reserved on every GPU that loads the library until the process
+ * exits.  When d_logits is NULL the logits are kept in that scratch, which
+ * holds at most NS_NOALLOC_MAX_LOGITS values: n * rows above that returns
+ * NS_ERR_ARG (pass d_logits for larger heads, e.g. the full vocabulary).
+ * The first call on each device looks up the scratch's device address and
+ * prepares the kernels for that device; make that first call before any
+ * stream capture.  Every call uses the same scratch and leaves its contents
+ * behind: calls that may overlap on the GPU (different streams without an
+ * ordering between them) race and must not be issued.
+ */
+#define NS_NOALLOC_MAX_LOGITS (1 << 20)
+NS_API ns_status ns_dense_lm_head_topk_noalloc(const uint16_t *d_W_head, int32_t rows, int32_t H,
+                                               const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
+                                               int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
+                                               ns_stream stream);
+
+/*
  * Device pointers into a sequence's state (owned by the handle; valid until
  * ns_destroy).  Any out-pointer may be NULL.
  *   ids     int32 [W_max]  I_t ascending (first *count entries valid)

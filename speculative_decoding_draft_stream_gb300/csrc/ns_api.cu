@@ -264,6 +264,17 @@ static ns_status check_gather_project_args(ns_handle *h, int32_t seq, const uint
   return NS_OK;
 }
 
+// Trace events are recorded as external event nodes when the stream is being
+// captured into a CUDA graph (so a captured step still times its kernels) and
+// as plain records otherwise (the external flag is only valid in capture).
+static cudaError_t trace_record(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess) return e;
+  if (cap == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  return cudaEventRecord(ev, st);
+}
+
 // Fused gather + projection, then top-k; `mid` (nullable) is recorded
 // between the two kernels.
 static cudaError_t enqueue_gather_project(ns_handle *h, int32_t seq, const uint16_t *d_W_head,
@@ -284,7 +295,7 @@ static cudaError_t enqueue_gather_project(ns_handle *h, int32_t seq, const uint1
   a.part = s.ppart;
   a.tickets = s.pticket;
   cudaError_t e = ns::launch_project(ns::kGatherRows, a, h->pgrid, cs);
-  if (e == cudaSuccess && mid) e = cudaEventRecordWithFlags(mid, cs, cudaEventRecordExternal);
+  if (e == cudaSuccess && mid) e = trace_record(mid, cs);
   if (e == cudaSuccess) e = ns::launch_topk(a.logits, a.ld, s.count, 0, s.active, n, k, d_ids, d_vals, cs);
   return e;
 }
@@ -297,12 +308,6 @@ ns_status ns_gather_sub_lm_head_topk(ns_handle *h, int32_t seq, const uint16_t *
   if (st != NS_OK) return st;
   return cuda_status(enqueue_gather_project(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids,
                                             d_topk_vals, static_cast<cudaStream_t>(stream), nullptr));
-}
-
-// Trace events are recorded as external event nodes when the stream is being
-// captured into a CUDA graph, so a captured step still times its kernels.
-static cudaError_t trace_record(cudaEvent_t ev, cudaStream_t st) {
-  return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
 }
 
 ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,

@@ -32,8 +32,9 @@ EXPORTED = (
     "ns_status_string", "ns_create", "ns_destroy", "ns_device_bytes", "ns_stream_init", "ns_stream_append",
     "ns_build_active_vocab", "ns_gather_head_rows", "ns_sub_lm_head_logits_topk", "ns_step",
     "ns_dense_lm_head_topk", "ns_get_active", "ns_get_state", "ns_get_error", "ns_state_update",
-    "ns_gather_sub_lm_head_topk", "ns_trace_events",
+    "ns_gather_sub_lm_head_topk", "ns_trace_events", "ns_dense_lm_head_topk_noalloc",
 )
+NOALLOC_MAX_LOGITS = 1 << 20
 
 
 class NanoSpecError(RuntimeError):
@@ -78,6 +79,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "ns_state_update": (I32, [P, I32, P, I32, P, I32, I32, P]),
         "ns_gather_sub_lm_head_topk": (I32, [P, I32, U16P, U16P, I32, I32, P, I32, P, P, P]),
         "ns_trace_events": (I32, [P, ctypes.POINTER(P), I32]),
+        "ns_dense_lm_head_topk_noalloc": (I32, [U16P, I32, I32, U16P, I32, I32, P, I32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -290,3 +292,31 @@ class Handle:
         f = ctypes.c_uint32()
         _check(self._lib.ns_get_error(self._h, ctypes.byref(f), int(clear)), "ns_get_error")
         return int(f.value)
+
+
+def dense_lm_head_topk_noalloc(W_head: torch.Tensor, rows: int, hidden: torch.Tensor, k: int,
+                               logits: Optional[torch.Tensor] = None, ids: Optional[torch.Tensor] = None,
+                               vals: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """ns_dense_lm_head_topk_noalloc: the dense head for callers that cannot allocate device memory.
+
+    No handle; the library allocates nothing and uses a fixed scratch array in
+    its own image.  Output tensors can be passed in (so nothing is allocated
+    here either).  Without `logits`, n * rows must not exceed
+    NOALLOC_MAX_LOGITS.  Calls that may overlap on the GPU share the scratch
+    and race.
+    """
+    lib = load_library()
+    n, H = hidden.shape
+    if ids is None:
+        ids = torch.empty((n, k), dtype=torch.int32, device=hidden.device)
+    if vals is None:
+        vals = torch.empty((n, k), dtype=torch.float32, device=hidden.device)
+    if logits is None and n * rows > NOALLOC_MAX_LOGITS:
+        raise NanoSpecError(-1, f"ns_dense_lm_head_topk_noalloc: n*rows = {n * rows} exceeds the scratch "
+                                f"({NOALLOC_MAX_LOGITS} logits); pass a logits tensor")
+    ld = logits.shape[1] if logits is not None else 0
+    _check(lib.ns_dense_lm_head_topk_noalloc(_ptr(W_head, _BF16, "W_head"), rows, H, _ptr(hidden, _BF16, "hidden"),
+                                             n, k, _ptr(logits, torch.float32, "logits"), ld,
+                                             _ptr(ids, torch.int32, "ids"), _ptr(vals, torch.float32, "vals"),
+                                             _stream(stream)), "ns_dense_lm_head_topk_noalloc")
+    return ids, vals
