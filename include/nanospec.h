@@ -212,10 +212,10 @@ NS_API ns_status ns_gather_sub_lm_head_topk(ns_handle *h, int32_t seq, const uin
  * event recording).  While set, ns_step records, on its stream,
  *   events[0] before its first kernel,
  *   events[1] after the state update (append + active vocabulary),
- *   events[2] after the fused gather + projection,
- *   events[3] after the top-k.
- * events must stay valid while set; n_events must be 4, or 0 with
- * events == NULL to switch tracing off.  The events are borrowed cudaEvent_t.
+ *   events[2] and events[3] after the fused gather + projection + top-k.
+ * Inside stream capture they become external event nodes.  events must stay
+ * valid while set; n_events must be 4, or 0 with events == NULL to switch
+ * tracing off.  The events are borrowed cudaEvent_t.
  */
 NS_API ns_status ns_trace_events(ns_handle *h, ns_event *events, int32_t n_events);
 

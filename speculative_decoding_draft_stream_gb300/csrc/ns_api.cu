@@ -77,6 +77,10 @@ void layout(ns_handle *h, Carver &cv) {
     s.first = c.K_pre > 0 ? cv.take<int32_t>(c.V) : nullptr;
     s.cand = c.K_pre > 0 ? cv.take<int32_t>((size_t)c.max_prompt * c.K_pre) : nullptr;
     s.sinit = cv.take<int32_t>((size_t)c.max_prompt * (1 + c.K_pre));
+    const size_t ncand = (size_t)ns::umma_tiles(c.W_max) * ns::kProjBN * c.max_k;
+    s.cand_v = cv.take<float>(ncand);
+    s.cand_i = cv.take<int32_t>(ncand);
+    s.slice_ticket = cv.take<int32_t>(ns::umma_cluster());
   }
   h->dense_ld = (c.V + 3) & ~3;
   h->dense_logits = cv.take<float>((size_t)ns::kProjBN * h->dense_ld);
@@ -118,7 +122,7 @@ ns_status ns_create(const ns_config *cfg, ns_handle **out) {
   h->cfg = c;
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
-      ns::prepare_project_kernels() != cudaSuccess) {
+      ns::prepare_project_kernels() != cudaSuccess || ns::prepare_umma_kernels() != cudaSuccess) {
     delete h;
     return NS_ERR_CUDA;
   }
@@ -275,28 +279,36 @@ static cudaError_t trace_record(cudaEvent_t ev, cudaStream_t st) {
   return cudaEventRecord(ev, st);
 }
 
-// Fused gather + projection, then top-k; `mid` (nullable) is recorded
-// between the two kernels.
+// Fused gather + projection + top-k (one tcgen05 kernel).  `mid` (nullable)
+// is recorded after it.  With `programmatic` the kernel may begin while the
+// preceding state update finishes.
 static cudaError_t enqueue_gather_project(ns_handle *h, int32_t seq, const uint16_t *d_W_head,
                                           const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
                                           int32_t ld_logits, int32_t *d_ids, float *d_vals, cudaStream_t cs,
-                                          cudaEvent_t mid) {
+                                          cudaEvent_t mid, bool programmatic) {
   const ns::SeqDev &s = h->seqs[seq];
-  ns::ProjArgs a{};
-  a.rows = d_W_head;
-  a.idx = s.active;
-  a.count_ptr = s.count;
-  a.packed_out = s.packed;
-  a.hid = d_hidden;
-  a.n = n;
-  a.H = h->cfg.H;
-  a.logits = d_logits ? d_logits : s.logits;
-  a.ld = d_logits ? ld_logits : h->dims.ld_scratch;
-  a.part = s.ppart;
-  a.tickets = s.pticket;
-  cudaError_t e = ns::launch_project(ns::kGatherRows, a, h->pgrid, cs);
+  ns::UmmaLaunch L{};
+  L.W = d_W_head;
+  L.V = h->cfg.V;
+  L.H = h->cfg.H;
+  L.hid = d_hidden;
+  L.n = n;
+  L.packed = s.packed;
+  L.W_max = h->cfg.W_max;
+  L.idx = s.active;
+  L.count_ptr = s.count;
+  L.k = k;
+  L.logits = d_logits ? d_logits : s.logits;
+  L.ld = d_logits ? ld_logits : h->dims.ld_scratch;
+  L.cand_v = s.cand_v;
+  L.cand_i = s.cand_i;
+  L.slice_ticket = s.slice_ticket;
+  L.out_ids = d_ids;
+  L.out_vals = d_vals;
+  L.err = h->err;
+  L.programmatic = programmatic;
+  cudaError_t e = ns::launch_umma_step(L, cs);
   if (e == cudaSuccess && mid) e = trace_record(mid, cs);
-  if (e == cudaSuccess) e = ns::launch_topk(a.logits, a.ld, s.count, 0, s.active, n, k, d_ids, d_vals, cs);
   return e;
 }
 
@@ -307,7 +319,7 @@ ns_status ns_gather_sub_lm_head_topk(ns_handle *h, int32_t seq, const uint16_t *
                                            d_topk_vals);
   if (st != NS_OK) return st;
   return cuda_status(enqueue_gather_project(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids,
-                                            d_topk_vals, static_cast<cudaStream_t>(stream), nullptr));
+                                            d_topk_vals, static_cast<cudaStream_t>(stream), nullptr, false));
 }
 
 ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
@@ -326,7 +338,7 @@ ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t 
   if (e == cudaSuccess && tr) e = trace_record(h->trace[1], cs);
   if (e == cudaSuccess)
     e = enqueue_gather_project(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals, cs,
-                               tr ? h->trace[2] : nullptr);
+                               tr ? h->trace[2] : nullptr, !tr);
   if (e == cudaSuccess && tr) e = trace_record(h->trace[3], cs);
   return cuda_status(e);
 }

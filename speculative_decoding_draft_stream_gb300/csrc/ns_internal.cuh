@@ -41,6 +41,9 @@ struct SeqDev {
   int32_t *first;     // [V] first flat index of an id in the prefill union (init only)
   int32_t *cand;      // [max_prompt x K_pre] prefill Top-K ids (init only)
   int32_t *sinit;     // [max_prompt x (1 + K_pre)] S_init entries (init only)
+  float *cand_v;      // [umma tiles x 64 x max_k] per-tile top-k candidates
+  int32_t *cand_i;
+  int32_t *slice_ticket;  // [umma cluster] arrival counters of the row slices
 };
 
 struct Dims {
@@ -180,5 +183,31 @@ cudaError_t launch_topk(const float *logits, int ld, const int32_t *count_ptr, i
 
 size_t project_smem_bytes();
 cudaError_t prepare_project_kernels();
+
+// Fused gather + projection + top-k on tcgen05 tensor cores (ns_umma.cu).
+struct UmmaLaunch {
+  const uint16_t *W;         // W_head [V x H]
+  int32_t V, H;
+  const uint16_t *hid;       // [n x H]
+  int32_t n;
+  uint16_t *packed;          // [W_max x H]
+  int32_t W_max;
+  const int32_t *idx;        // I_t
+  const int32_t *count_ptr;  // |I_t|
+  int32_t k;
+  float *logits;             // [n x ld]
+  int32_t ld;
+  float *cand_v;             // [umma_tiles(W_max) x 64 x k]
+  int32_t *cand_i;
+  int32_t *slice_ticket;     // [umma_cluster()]
+  int32_t *out_ids;          // [n x k]
+  float *out_vals;
+  uint32_t *err;
+  bool programmatic;         // may start while the preceding kernel finishes
+};
+int umma_tiles(int W_max);
+int umma_cluster();
+cudaError_t prepare_umma_kernels();
+cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st);
 
 }  // namespace ns

@@ -239,6 +239,10 @@ __global__ void __launch_bounds__(kStateThreads) append_kernel(SeqDev s, Dims d,
     }
   }
 
+  // Only this CTA is left: let a programmatically launched successor start
+  // its prologue; it waits for this grid's results before reading them.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   // ---- C_draft: distinct valid tree ids in first-occurrence order ----------
   if (tid < n_tree) s_tree[tid] = tree[tid];
   __syncthreads();

@@ -1,0 +1,550 @@
+// Fused sub-head step on the 5th-generation tensor cores: gather of
+// W_head[I_t, :] into the packed buffer, projection of the draft hidden
+// states through it, and per-row top-k remapped to global ids
+// (MicroSpec §3.3 gathering into a contiguous buffer + dense product; §3.1
+// Eq. 1 restricted to the active rows).
+//
+// Tile: 128 W_head rows (UMMA M) x 64 hidden rows (UMMA N, n <= 64).
+// Each tile belongs to one cluster of 8 CTAs that split H eight ways; the
+// 64-wide k slices are dealt round-robin (CTA c takes slices c, c+8, ...),
+// so at any moment a cluster reads 1 KB runs of each row.
+// Per CTA and per k slice (a 4-stage ring overlaps the roles):
+//   * warps 4-7 gather the tile's 128 rows with 16-byte cp.async (four rows
+//     of 128 contiguous bytes per warp instruction) into the 128-byte-
+//     swizzled operand layout, then fence the async proxy and arrive on the
+//     stage's "full" barrier;
+//   * warp 0 (one lane) loads the hidden slice with a tiled TMA load onto the
+//     same barrier;
+//   * warp 1 (one lane) issues four tcgen05.mma (K = 16 each) into a
+//     128 x 64 fp32 accumulator in tensor memory and commits to the stage's
+//     "empty" barrier;
+//   * warp 2 (one lane) stores the gathered stage to the packed buffer with a
+//     TMA tile store, so each W_head row crosses HBM once per step.
+// Epilogue: warps 4-7 read the accumulator (tcgen05.ld, one row per thread),
+// every CTA publishes its partial tile in shared memory, and after a cluster
+// barrier CTA c adds the eight partials for hidden rows [8c, 8c+8) through
+// distributed shared memory in a fixed order (deterministic), ranks each
+// row's 128 columns (one warp per row) and writes those logits.  The
+// per-tile candidates of a row slice are merged by the last CTA of that slice
+// to finish (atomic ticket) into the final top-k.
+//
+// Every wait is bounded (about a second); a wait that runs out sets
+// NS_FLAG_TIMEOUT and the kernel still follows the same barrier sequence and
+// frees its tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "ns_internal.cuh"
+
+namespace ns {
+namespace {
+
+constexpr int kUM = 128;                     // W rows per tile
+constexpr int kUN = 64;                      // hidden rows per tile
+constexpr int kUK = 64;                      // k per stage: one 128-byte swizzled row
+constexpr int kUStages = 4;
+constexpr int kUCluster = 8;                 // K splits per tile = CTAs per cluster
+constexpr int kUThreads = 256;
+constexpr int kGatherThreads = 128;          // warps 4-7
+constexpr int kInFlight = 3;                 // cp.async stages a gather thread keeps in flight
+constexpr int kStoresInFlight = 1;           // packed-buffer stores still reading a stage
+// A stage is published kInFlight-1 iterations after it is issued and released
+// by the store issuer kStoresInFlight stores later; the gather threads wait for
+// the release of the stage they reuse kUStages iterations on.  Reuse can only
+// make progress when the two lags fit in the ring.
+static_assert((kInFlight - 1) + kStoresInFlight <= kUStages - 1, "stage ring too short for the pipeline lags");
+constexpr int kSlice = kUN / kUCluster;      // hidden rows reduced by one CTA
+constexpr int kStageA = kUM * kUK * 2;       // 16 KB
+constexpr int kStageB = kUN * kUK * 2;       // 8 KB
+constexpr int kStage = kStageA + kStageB;    // 24 KB (1024-byte multiple)
+constexpr int kRingBytes = kUStages * kStage;
+constexpr int kPartBytes = kUN * kUM * 4;    // one CTA's partial tile, [r][j] fp32
+constexpr int kMiscBytes = 1024;             // barriers, TMEM slot, ticket flag, row ids
+constexpr int kUSmem = kRingBytes + kMiscBytes + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = 64;
+constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
+
+static_assert(kPartBytes + kSlice * kUM * 4 + 2 * kSlice * NS_MAX_TOPK * 4 <= kRingBytes,
+              "epilogue buffers reuse the stage ring");
+
+// D = fp32, A = B = bf16, both K-major, N = 64, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kUN >> 3) << 17) |
+                            ((uint32_t)(kUM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier ---------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a phase; false (and NS_FLAG_TIMEOUT) when it runs out.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(err, NS_FLAG_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// ---- TMA ------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch(const CUtensorMap *m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// ---- tcgen05 ----------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (sm_100 descriptor version 1).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;             // leading byte offset (unused with a 128-byte swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
+  d |= (uint64_t)1 << 46;             // descriptor version
+  d |= (uint64_t)2 << 61;             // SWIZZLE_128B
+  return d;
+}
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---- cluster ----------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_peer_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+struct UmmaArgs {
+  const uint16_t *W;         // W_head [V x H]
+  const int32_t *idx;        // I_t ascending
+  const int32_t *count_ptr;  // |I_t|
+  int32_t H, n, k;
+  float *logits;             // [n x ld]
+  int32_t ld;
+  float *cand_v;             // [tiles x 64 x k] per-tile candidates
+  int32_t *cand_i;
+  int32_t *slice_ticket;     // [kUCluster]
+  int32_t *out_ids;          // [n x k]
+  float *out_vals;
+  uint32_t *err;
+};
+
+template <int KMAX>
+__global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1)
+    umma_step_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmP,
+                     UmmaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte-swizzled tiles need 1024-byte alignment
+  uint8_t *gbase = smem_raw + (base - raw);
+  const uint32_t bar_full = base + kRingBytes;
+  const uint32_t bar_empty = bar_full + 8 * kUStages;
+  const uint32_t bar_acc = bar_empty + 8 * kUStages;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kRingBytes + 16 * kUStages + 8);
+  int *s_flag = reinterpret_cast<int *>(gbase + kRingBytes + 16 * kUStages + 16);
+  int *s_rows = reinterpret_cast<int *>(gbase + kRingBytes + 256);  // 128 row ids
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = cluster_rank();
+  const int tile = blockIdx.x / kUCluster;
+
+  // ---- prologue (overlaps the state update when launched programmatically) --
+  if (tid == 0) {
+    tma_prefetch(&tmH);
+    tma_prefetch(&tmP);
+    for (int s = 0; s < kUStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1 + kGatherThreads);  // the TMA issuer and every gather thread
+      mbar_init(bar_empty + 8 * s, 2);                  // the MMA commit and the packed-store issuer
+    }
+    mbar_init(bar_acc, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  grid_dependency_wait();  // I_t and |I_t| come from the state update
+  const int m = *a.count_ptr;
+  const int T = (m + kUM - 1) / kUM;
+  if (tile >= T) {  // uniform across the cluster
+    if (T == 0 && tile == 0) {
+      const int r = (int)crank * kSlice + warp;
+      if (warp < kSlice && r < a.n && lane < a.k) {
+        a.out_ids[r * a.k + lane] = -1;
+        a.out_vals[r * a.k + lane] = -__int_as_float(0x7f800000);
+      }
+    }
+    __syncwarp();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
+
+  const int KC = a.H / kUK;
+  // k slices of this CTA: crank, crank + 8, ... (nk of them)
+  const int nk = KC > (int)crank ? (KC - (int)crank + kUCluster - 1) / kUCluster : 0;
+  const int row0 = tile * kUM;
+  if (tid < kUM) {
+    const int j = row0 + tid;
+    s_rows[tid] = a.idx[j < m ? j : m - 1];  // rows past |I_t| repeat the last active row
+  }
+  __syncthreads();
+
+  // ---- main loop -------------------------------------------------------------
+  if (warp == 0 && lane == 0) {  // hidden slices by TMA
+    int issued = 0;
+    for (int kt = 0; kt < nk; ++kt) {
+      const int s = kt % kUStages;
+      if (kt >= kUStages && !mbar_wait(bar_empty + 8 * s, ((kt / kUStages) - 1) & 1, a.err)) break;
+      issued = kt + 1;
+      mbar_expect_tx(bar_full + 8 * s, kStageB);
+      tma_load_2d(base + s * kStage + kStageA, &tmH, ((int)crank + kt * kUCluster) * kUK, 0, bar_full + 8 * s);
+    }
+    // nothing may still be landing in shared memory when the CTA leaves
+    const int first = issued > kUStages ? issued - kUStages : 0;
+    for (int kt = first; kt < issued; ++kt) mbar_wait(bar_full + 8 * (kt % kUStages), (kt / kUStages) & 1, a.err);
+  } else if (warp >= 4) {  // W_head rows by cp.async
+    const int p = tid - 128, wl = p >> 5, c = lane & 7;
+    int arrived = 0;
+    for (int kt = 0; kt < nk; ++kt) {
+      const int s = kt % kUStages;
+      if (kt >= kUStages) mbar_wait(bar_empty + 8 * s, ((kt / kUStages) - 1) & 1, a.err);
+      const uint32_t A = base + s * kStage;
+      const int col = ((int)crank + kt * kUCluster) * kUK + c * 8;
+#pragma unroll
+      for (int it = 0; it < kUM / 16; ++it) {
+        const int row = it * 16 + wl * 4 + (lane >> 3);
+        const uint16_t *src = a.W + (size_t)s_rows[row] * a.H + col;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(A + row * 128 + ((c ^ (row & 7)) << 4)),
+                     "l"(src)
+                     : "memory");
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      if (kt + 1 - arrived >= kInFlight) {  // the oldest pending stage has landed: publish it
+        asm volatile("cp.async.wait_group %0;" ::"n"(kInFlight - 1) : "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(bar_full + 8 * (arrived % kUStages));
+        ++arrived;
+      }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    for (; arrived < nk; ++arrived) mbar_arrive(bar_full + 8 * (arrived % kUStages));
+  } else if (warp == 1 && lane == 0) {
+    bool ok = true;
+    for (int kt = 0; kt < nk && ok; ++kt) {
+      const int s = kt % kUStages;
+      ok = mbar_wait(bar_full + 8 * s, (kt / kUStages) & 1, a.err);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t A = base + s * kStage;
+#pragma unroll
+      for (int kk = 0; kk < kUK / 16; ++kk)
+        umma_bf16(tmem, sw128_desc(A + kk * 32), sw128_desc(A + kStageA + kk * 32), (kt | kk) != 0);
+      umma_commit(bar_empty + 8 * s);
+    }
+    if (nk > 0 && ok) umma_commit(bar_acc);
+    else mbar_arrive(bar_acc);
+  } else if (warp == 2 && lane == 0) {
+    int released = 0;
+    for (int kt = 0; kt < nk; ++kt) {
+      const int s = kt % kUStages;
+      if (!mbar_wait(bar_full + 8 * s, (kt / kUStages) & 1, a.err)) break;
+      tma_store_2d(&tmP, base + s * kStage, ((int)crank + kt * kUCluster) * kUK, row0);
+      bulk_commit();
+      if (kt + 1 - released > kStoresInFlight) {  // the oldest store has read its stage
+        asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kStoresInFlight) : "memory");
+        mbar_arrive(bar_empty + 8 * (released % kUStages));
+        ++released;
+      }
+    }
+    bulk_wait_read_all();
+    for (; released < nk; ++released) mbar_arrive(bar_empty + 8 * (released % kUStages));
+    bulk_wait_all();
+  }
+
+  // ---- epilogue: accumulator -> partial tile in shared memory ---------------
+  float v[kUN];
+  if (warp >= 4) {
+    // tcgen05.ld is warp-collective: the whole warp takes the same branch
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_acc, 0, a.err));
+    tc_fence_after();
+    if (nk > 0 && ok) {
+      const uint32_t t0 = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+#pragma unroll
+      for (int c = 0; c < kUN; c += 16) tmem_ld16(t0 + c, v + c);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int c = 0; c < kUN; ++c) v[c] = 0.f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();  // MMAs, TMEM reads and packed stores are all done with the ring
+  __syncwarp();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  float *P = reinterpret_cast<float *>(gbase);  // [64][128] partial of this CTA
+  if (warp >= 4) {
+    const int j = (warp - 4) * 32 + lane;
+#pragma unroll
+    for (int r = 0; r < kUN; ++r) P[r * kUM + j] = v[r];
+  }
+  __syncwarp();
+  cluster_sync();
+
+  // ---- reduce hidden rows [8c, 8c+8) over the eight partials ---------------
+  float *F = reinterpret_cast<float *>(gbase + kPartBytes);  // [8][128]
+  {
+    const int rr = tid / (kUM / 4), j = (tid % (kUM / 4)) * 4;  // 256 threads cover 8 x 128
+    const uint32_t off = base + (uint32_t)(((crank * kSlice + rr) * kUM + j) * 4);
+    float4 s4 = ld_peer_f4(map_peer(off, 0));
+#pragma unroll
+    for (uint32_t p = 1; p < kUCluster; ++p) {
+      const float4 q = ld_peer_f4(map_peer(off, p));
+      s4.x += q.x;
+      s4.y += q.y;
+      s4.z += q.z;
+      s4.w += q.w;
+    }
+    *reinterpret_cast<float4 *>(F + rr * kUM + j) = s4;
+  }
+  __syncthreads();
+
+  // ---- per-tile top-k of each row (one warp per hidden row) -----------------
+  // Candidates carry global ids (I_t is ascending, so id order = column order).
+  const int r = (int)crank * kSlice + warp;
+  if (r < a.n) {
+    TopList<4> L;
+    L.clear();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = lane + 32 * q;
+      if (row0 + j < m) L.insert(F[warp * kUM + j], s_rows[j]);
+    }
+    const size_t o = ((size_t)tile * kUN + r) * a.k;
+    warp_select<4>(L, a.k, a.cand_v + o, a.cand_i + o);
+    if (lane == 0) __threadfence();  // candidates visible before the ticket
+  }
+  __syncthreads();
+  if (tid == 0) {
+    *s_flag = (atomicAdd(a.slice_ticket + crank, 1) == T - 1);
+    __threadfence();
+  }
+  for (int i = tid; i < kSlice * kUM; i += kUThreads) {
+    const int rr = i / kUM, j = i % kUM;
+    const int rw = (int)crank * kSlice + rr, jg = row0 + j;
+    if (rw < a.n && jg < m) a.logits[(size_t)rw * a.ld + jg] = F[i];
+  }
+  __syncthreads();
+  if (*s_flag) {  // last tile of this row slice: merge every tile's candidates
+    if (tid == 0) a.slice_ticket[crank] = 0;
+    if (r < a.n) {
+      // each lane takes the (sorted) lists of tiles lane, lane + 32, ...
+      TopList<KMAX> M;
+      M.clear();
+      for (int t = lane; t < T; t += 32) {
+        const size_t o = ((size_t)t * kUN + r) * a.k;
+        float cv[KMAX];
+        int ci[KMAX];
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q) {  // all loads first, then the inserts
+          cv[q] = q < a.k ? __ldcg(a.cand_v + o + q) : -__int_as_float(0x7f800000);
+          ci[q] = q < a.k ? __ldcg(a.cand_i + o + q) : kEmptyId;
+        }
+        if (t == lane) {  // the first list is already sorted
+#pragma unroll
+          for (int q = 0; q < KMAX; ++q) {
+            M.v[q] = cv[q];
+            M.id[q] = ci[q];
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < KMAX; ++q) M.insert(cv[q], ci[q]);
+        }
+      }
+      float *wv = reinterpret_cast<float *>(gbase + kPartBytes + kSlice * kUM * 4) + warp * NS_MAX_TOPK;
+      int *wi = reinterpret_cast<int *>(gbase + kPartBytes + kSlice * kUM * 4 + kSlice * NS_MAX_TOPK * 4) +
+                warp * NS_MAX_TOPK;
+      warp_select<KMAX>(M, a.k, wv, wi);
+      __syncwarp();
+      if (lane < a.k) {
+        const int id = wi[lane];
+        const bool ok = id != kEmptyId;
+        a.out_ids[r * a.k + lane] = ok ? id : -1;
+        a.out_vals[r * a.k + lane] = ok ? wv[lane] : -__int_as_float(0x7f800000);
+      }
+    }
+  }
+  __syncwarp();
+  cluster_sync();  // peers may still be reading this CTA's partial tile
+}
+
+// ---- host side ---------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// 2-D bf16 tensor [outer x inner] with rows of `inner` elements, 128-byte swizzle.
+bool encode_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                    uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int umma_tiles(int W_max) { return (W_max + kUM - 1) / kUM; }
+int umma_cluster() { return kUCluster; }
+
+cudaError_t prepare_umma_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(umma_step_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(umma_step_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
+  if (e == cudaSuccess && !encoder()) e = cudaErrorNotSupported;
+  return e;
+}
+
+cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
+  CUtensorMap tmH, tmP;
+  if (!encode_bf16_2d(&tmH, L.hid, L.H, L.n, kUK, kUN) || !encode_bf16_2d(&tmP, L.packed, L.H, L.W_max, kUK, kUM))
+    return cudaErrorInvalidValue;
+  UmmaArgs a{};
+  a.W = L.W;
+  a.idx = L.idx;
+  a.count_ptr = L.count_ptr;
+  a.H = L.H;
+  a.n = L.n;
+  a.k = L.k;
+  a.logits = L.logits;
+  a.ld = L.ld;
+  a.cand_v = L.cand_v;
+  a.cand_i = L.cand_i;
+  a.slice_ticket = L.slice_ticket;
+  a.out_ids = L.out_ids;
+  a.out_vals = L.out_vals;
+  a.err = L.err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(umma_tiles(L.W_max) * kUCluster));
+  cfg.blockDim = dim3(kUThreads);
+  cfg.dynamicSmemBytes = kUSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = L.programmatic ? 1 : 0;
+  if (L.k <= 16) return cudaLaunchKernelEx(&cfg, umma_step_kernel<16>, tmH, tmP, a);
+  return cudaLaunchKernelEx(&cfg, umma_step_kernel<32>, tmH, tmP, a);
+}
+
+}  // namespace ns

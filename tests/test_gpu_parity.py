@@ -105,6 +105,22 @@ def test_mid_every_step(pkg, fused):
     _run_workload(pkg, MID, fused)
 
 
+# Full-width heads on a small vocabulary: H = 4096 and 3584 give every CTA of
+# the fused kernel more k slices than its stage ring holds, so stages are
+# reused (the Llama-3 and Qwen-2.5 widths), with ragged last tiles.
+WIDE = [
+    WorkloadConfig(name="h4096", V=30011, H=4096, W_max=700, K_pre=3, K_ver=3, prompt_len=500, self_copy=0.4,
+                   zipf_s=1.05, steps=6, n_tree=60, tree_local=0.7, tree_recent=256, n_verify=2),
+    WorkloadConfig(name="h3584", V=9001, H=3584, W_max=333, K_pre=3, K_ver=3, prompt_len=200, self_copy=0.4,
+                   zipf_s=1.05, steps=5, n_tree=45, tree_local=0.7, tree_recent=128, n_verify=1),
+]
+
+
+@pytest.mark.parametrize("cfg", WIDE, ids=lambda c: c.name)
+def test_wide_heads_every_step(pkg, cfg):
+    _run_workload(pkg, cfg, True)
+
+
 EDGE = [
     # tiny vocabulary and window; |I_t| < k pads the top-k
     WorkloadConfig(name="tiny", V=64, H=64, W_max=4, K_pre=1, K_ver=2, prompt_len=9, self_copy=0.3, zipf_s=1.0,
