@@ -66,6 +66,7 @@ typedef int32_t ns_status;
 #define NS_FLAG_BAD_ID 0x1u    /* an input token id outside [0, V) was skipped */
 #define NS_FLAG_OVERFLOW 0x2u  /* an internal capacity was exceeded (bug)      */
 #define NS_FLAG_TIMEOUT 0x4u   /* a bounded device-side wait gave up            */
+#define NS_FLAG_INTERNAL 0x8u  /* an internal id was out of range and skipped (a bug); bits 8..15 name the site */
 
 typedef void *ns_stream; /* cudaStream_t */
 typedef void *ns_event;  /* cudaEvent_t  */

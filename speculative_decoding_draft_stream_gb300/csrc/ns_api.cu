@@ -17,7 +17,6 @@ struct ns_handle {
   ns::Dims dims;
   int device = 0;
   int num_sms = 0;
-  int vgrid = 1;  // CTAs of the verify Top-K
   int pgrid = 1;  // CTAs of the projection
   int ggrid = 1;  // CTAs of the gather
   char *base = nullptr;
@@ -69,9 +68,6 @@ void layout(ns_handle *h, Carver &cv) {
     s.length = cv.take<long long>(1);
     s.packed = cv.take<uint16_t>((size_t)c.W_max * c.H);
     s.logits = cv.take<float>((size_t)ns::kProjBN * d.ld_scratch);
-    s.vpart_v = cv.take<float>((size_t)h->vgrid * NS_MAX_SELECT_K);
-    s.vpart_i = cv.take<int32_t>((size_t)h->vgrid * NS_MAX_SELECT_K);
-    s.vticket = cv.take<int32_t>(1);
     s.ppart = cv.take<float>((size_t)h->pgrid * ns::kProjBN * ns::kProjBM);
     s.pticket = cv.take<int32_t>(h->pgrid);
     s.first = c.K_pre > 0 ? cv.take<int32_t>(c.V) : nullptr;
@@ -135,9 +131,10 @@ ns_status ns_create(const ns_config *cfg, ns_handle **out) {
   d.nwords = (c.V + 31) / 32;
   d.nwords_pad = (d.nwords + 3) & ~3;
   d.ld_scratch = (c.W_max + 3) & ~3;
-  const int per_cta = 4 * ns::kStateThreads;  // one float4 per thread
-  h->vgrid = (c.V + per_cta - 1) / per_cta;
-  if (h->vgrid > h->num_sms) h->vgrid = h->num_sms;
+  if (ns::prepare_state_kernels(&d) != cudaSuccess) {
+    delete h;
+    return NS_ERR_CUDA;
+  }
   h->pgrid = 2 * h->num_sms;
   h->ggrid = 4 * h->num_sms;
 
@@ -196,7 +193,7 @@ ns_status ns_stream_append(ns_handle *h, int32_t seq, const int32_t *d_tree_ids,
   ns_status st = check_append_args(h, seq, d_tree_ids, n_tree, d_verify_logits, n_verify, verify_row);
   if (st != NS_OK) return st;
   const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
-  return cuda_status(ns::launch_append(h->seqs[seq], h->dims, h->vgrid, d_tree_ids, n_tree, zrow, false, h->err,
+  return cuda_status(ns::launch_append(h->seqs[seq], h->dims, d_tree_ids, n_tree, zrow, false, h->err,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -254,7 +251,7 @@ ns_status ns_state_update(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, 
   ns_status st = check_append_args(h, seq, d_tree_ids, n_tree, d_verify_logits, n_verify, verify_row);
   if (st != NS_OK) return st;
   const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
-  return cuda_status(ns::launch_append(h->seqs[seq], h->dims, h->vgrid, d_tree_ids, n_tree, zrow, true, h->err,
+  return cuda_status(ns::launch_append(h->seqs[seq], h->dims, d_tree_ids, n_tree, zrow, true, h->err,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -334,7 +331,7 @@ ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t 
   const bool tr = h->tracing;
   cudaError_t e = tr ? trace_record(h->trace[0], cs) : cudaSuccess;
   const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
-  if (e == cudaSuccess) e = ns::launch_append(h->seqs[seq], h->dims, h->vgrid, d_tree_ids, n_tree, zrow, true, h->err, cs);
+  if (e == cudaSuccess) e = ns::launch_append(h->seqs[seq], h->dims, d_tree_ids, n_tree, zrow, true, h->err, cs);
   if (e == cudaSuccess && tr) e = trace_record(h->trace[1], cs);
   if (e == cudaSuccess)
     e = enqueue_gather_project(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals, cs,

@@ -33,9 +33,6 @@ struct SeqDev {
   long long *length;  // [1] |S|
   uint16_t *packed;   // [W_max x H] bf16 rows W_head[I_t[j], :]
   float *logits;      // [kProjBN x ld_scratch] fp32 logits when the caller passes none
-  float *vpart_v;     // [vgrid x NS_MAX_SELECT_K] verify top-K partials
-  int32_t *vpart_i;
-  int32_t *vticket;   // [1] arrival counter of the verify kernel
   float *ppart;       // [proj_grid x kProjBN x kProjBM] split-K partial tiles
   int32_t *pticket;   // [proj_grid] per-tile arrival counters
   int32_t *first;     // [V] first flat index of an id in the prefill union (init only)
@@ -48,6 +45,7 @@ struct SeqDev {
 
 struct Dims {
   int32_t V, H, W_max, K_pre, K_ver, nwords, nwords_pad, ld_scratch;
+  int32_t state_cluster;  // CTAs of the state-update cluster (16 where the device allows, else 8)
 };
 
 // ---------------------------------------------------------------------------
@@ -148,6 +146,62 @@ __device__ void block_select(TopList<KMAX> &L, int K, float *sc_v, int *sc_i, fl
   __syncthreads();
 }
 
+// Warp-wide streaming Top-K (K <= 32).  Lane q < K holds the q-th best value
+// pushed so far (larger value first, then smaller id); (tv, ti) is the K-th
+// best, uniform across the warp.  Each push hands one value per lane; a value
+// costs a compare and a vote unless it beats the K-th best, which is rare, and
+// only then is it merged into the lane-distributed list.
+struct WarpStreamTopK {
+  float lv, tv;
+  int li, ti, K;
+  __device__ __forceinline__ void init(int k) {
+    K = k;
+    lv = tv = -__int_as_float(0x7f800000);
+    li = ti = kEmptyId;
+  }
+  __device__ __forceinline__ void push(float x, int i) {
+    const int lane = threadIdx.x & (kWarp - 1);
+    unsigned m = __ballot_sync(0xffffffffu, better(x, i, tv, ti));
+    while (m) {
+      const int src = __ffs(m) - 1;
+      m &= m - 1;
+      const float cx = __shfl_sync(0xffffffffu, x, src);
+      const int ci = __shfl_sync(0xffffffffu, i, src);
+      if (!better(cx, ci, tv, ti)) continue;  // the threshold rose since the vote
+      const int pos = __popc(__ballot_sync(0xffffffffu, lane < K && better(lv, li, cx, ci)));
+      const float uv = __shfl_up_sync(0xffffffffu, lv, 1);
+      const int ui = __shfl_up_sync(0xffffffffu, li, 1);
+      if (lane < K && lane > pos) {
+        lv = uv;
+        li = ui;
+      } else if (lane == pos) {
+        lv = cx;
+        li = ci;
+      }
+      tv = __shfl_sync(0xffffffffu, lv, K - 1);
+      ti = __shfl_sync(0xffffffffu, li, K - 1);
+    }
+  }
+};
+
+// Sorts one (value, id) per lane across the warp, best first (bitonic network).
+__device__ __forceinline__ void warp_sort_desc(float &v, int &i) {
+  const int lane = threadIdx.x & (kWarp - 1);
+#pragma unroll
+  for (int k = 2; k <= kWarp; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, j);
+      const int oi = __shfl_xor_sync(0xffffffffu, i, j);
+      const bool take_better = ((lane & j) == 0) == ((lane & k) == 0);
+      if (take_better ? better(ov, oi, v, i) : better(v, i, ov, oi)) {
+        v = ov;
+        i = oi;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void set_flag(uint32_t *err, uint32_t f) { atomicOr(err, f); }
 
 // ---------------------------------------------------------------------------
@@ -155,8 +209,10 @@ __device__ __forceinline__ void set_flag(uint32_t *err, uint32_t f) { atomicOr(e
 // ---------------------------------------------------------------------------
 cudaError_t launch_init(const SeqDev &s, const Dims &d, const int32_t *prompt, int L, const float *prefill,
                         uint32_t *err, cudaStream_t st);
-cudaError_t launch_append(const SeqDev &s, const Dims &d, int vgrid, const int32_t *tree, int n_tree,
+cudaError_t launch_append(const SeqDev &s, const Dims &d, const int32_t *tree, int n_tree,
                           const float *verify_row_ptr, bool build, uint32_t *err, cudaStream_t st);
+// Sets the state kernels' shared-memory limits and picks d->state_cluster.
+cudaError_t prepare_state_kernels(Dims *d);
 cudaError_t launch_build(const SeqDev &s, const Dims &d, uint32_t *err, cudaStream_t st);
 cudaError_t launch_gather(const SeqDev &s, const Dims &d, const uint16_t *W, int grid, cudaStream_t st);
 

@@ -13,12 +13,12 @@
 // i.e. id in Unique(Suffix(S, W_max)).  Appending entry p overwrites the slot
 // of entry p - W_max, which is exactly the entry that leaves the window.
 #include "ns_internal.cuh"
+#include "ns_ptx.cuh"
 
 namespace ns {
 namespace {
 
 constexpr int kMaxAppend = NS_MAX_ROWS + NS_MAX_SELECT_K;
-constexpr int kCompactPerThread = 4;  // uint4 bitmap chunks per thread in one CTA
 
 __device__ __forceinline__ int warp_inclusive_scan(int v) {
   const int lane = threadIdx.x & (kWarp - 1);
@@ -51,43 +51,139 @@ __device__ int block_exclusive_scan(int v, int *sh, int *total) {
   return warp_off + incl - v;
 }
 
-// I_t = set bits of the bitmap in ascending order, by one CTA: each thread
-// pop-counts a contiguous run of words, a block scan gives every thread its
-// output offset, and each thread emits its ids in order.
-__device__ void compact_bitmap(const uint32_t *bitmap, int nwords_pad, int32_t *active, int32_t *count,
-                               int W_max, uint32_t *err, int *sh_scan) {
-  const int nw4 = nwords_pad / 4;
-  const int per = (nw4 + blockDim.x - 1) / blockDim.x;  // <= kCompactPerThread (host checks V)
-  const int v0 = threadIdx.x * per;
-  uint4 w[kCompactPerThread];
-  int c = 0;
+// I_t = set bits of the bitmap (in shared memory) in ascending order, by one
+// CTA of kStateThreads threads, in two phases.
+//  Scan: thread t takes G consecutive groups of four words (a contiguous run
+//  of 128 * G ids); one block scan of the per-thread counts of set bits and
+//  of nonzero words lists every nonzero word, in order, with the output
+//  offset of its first id (nz_w / nz_o, shared, nwords_pad ints each).
+//  Emit: the listed words are dealt so that neighbouring entries go to
+//  different warps (the dense run of frequent low ids is spread over all
+//  warps) and the lanes of a warp read different banks.  A thread writes the
+//  ids of a sparse word itself; the lanes of a warp write a dense word's ids
+//  together, one bit each.
+// Most words are zero when |I_t| << V; only the listed ones cost work after
+// the scan.  With `stage` (shared, W_max ints) the ids are gathered there and
+// copied to `active` with coalesced stores; without it they go straight to
+// `active`.
+constexpr int kCompactMaxG = 4;   // groups of four words per thread (V <= 4 * 4 * 1024 * 32)
+constexpr int kDenseBits = 8;     // a word with more set bits is emitted by its whole warp
+constexpr int kStageMaxW = 8192;  // largest W_max whose I_t is staged in shared memory
+static_assert(kStateThreads == kWarp * kWarp, "the block scan takes one warp of warp totals");
+
+__device__ void compact_bitmap(const uint32_t *bits, int nwords, int nwords_pad, int32_t *nz_w, int32_t *nz_o,
+                               int32_t *stage, int32_t *active, int32_t *count, int W_max, uint32_t *err,
+                               int *sh /* 2 * kWarp ints */) {
+  const int T = kStateThreads, tid = threadIdx.x;
+  const int lane = tid & (kWarp - 1), warp = tid / kWarp;
+  const int ng = nwords_pad / 4;
+  const int G = (ng + T - 1) / T;
+  const uint4 *bits4 = reinterpret_cast<const uint4 *>(bits);
+  uint4 w4[kCompactMaxG];
+  int cb = 0, cn = 0;  // set bits, nonzero words
 #pragma unroll
-  for (int q = 0; q < kCompactPerThread; ++q) {
-    w[q] = make_uint4(0u, 0u, 0u, 0u);
-    if (q < per && v0 + q < nw4) w[q] = __ldcg(reinterpret_cast<const uint4 *>(bitmap) + v0 + q);
-    c += __popc(w[q].x) + __popc(w[q].y) + __popc(w[q].z) + __popc(w[q].w);
+  for (int g = 0; g < kCompactMaxG; ++g) {
+    w4[g] = make_uint4(0u, 0u, 0u, 0u);
+    const int gi = tid * G + g;
+    if (g < G && gi < ng) {
+      w4[g] = bits4[gi];
+      cb += __popc(w4[g].x) + __popc(w4[g].y) + __popc(w4[g].z) + __popc(w4[g].w);
+      cn += (w4[g].x != 0u) + (w4[g].y != 0u) + (w4[g].z != 0u) + (w4[g].w != 0u);
+    }
   }
-  int total;
-  int pos = block_exclusive_scan(c, sh_scan, &total);
+  int ib = cb, in = cn;  // inclusive warp scans of both counts
 #pragma unroll
-  for (int q = 0; q < kCompactPerThread; ++q) {
-    const uint32_t ws[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+  for (int d = 1; d < kWarp; d <<= 1) {
+    const int xb = __shfl_up_sync(0xffffffffu, ib, d), xn = __shfl_up_sync(0xffffffffu, in, d);
+    if (lane >= d) {
+      ib += xb;
+      in += xn;
+    }
+  }
+  if (lane == kWarp - 1) {
+    sh[warp] = ib;
+    sh[kWarp + warp] = in;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int vb = sh[lane], vn = sh[kWarp + lane];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      uint32_t bits = ws[e];
-      const int base = ((v0 + q) * 4 + e) * 32;
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1;
-        if (pos < W_max) active[pos] = base + b;
-        ++pos;
+    for (int d = 1; d < kWarp; d <<= 1) {
+      const int xb = __shfl_up_sync(0xffffffffu, vb, d), xn = __shfl_up_sync(0xffffffffu, vn, d);
+      if (lane >= d) {
+        vb += xb;
+        vn += xn;
+      }
+    }
+    sh[lane] = vb;
+    sh[kWarp + lane] = vn;
+  }
+  __syncthreads();
+  const int total = sh[kWarp - 1], n_nz = sh[2 * kWarp - 1];
+  int ob = (warp > 0 ? sh[warp - 1] : 0) + ib - cb;
+  int on = (warp > 0 ? sh[kWarp + warp - 1] : 0) + in - cn;
+#pragma unroll
+  for (int g = 0; g < kCompactMaxG; ++g) {
+    if (g < G && (w4[g].x | w4[g].y | w4[g].z | w4[g].w) != 0u) {
+      const uint32_t ws[4] = {w4[g].x, w4[g].y, w4[g].z, w4[g].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (ws[e] != 0u) {
+          nz_w[on] = 4 * (tid * G + g) + e;
+          nz_o[on] = ob;
+          ++on;
+          ob += __popc(ws[e]);
+        }
       }
     }
   }
-  if (threadIdx.x == 0) {
-    if (total > W_max) set_flag(err, NS_FLAG_OVERFLOW);
-    *count = total < W_max ? total : W_max;
+  __syncthreads();
+  int32_t *out = stage != nullptr ? stage : active;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int r = 0; r * T < n_nz; ++r) {
+    const int k = r * T + kWarp * lane + ((warp + lane) & (kWarp - 1));
+    const int w = k < n_nz ? nz_w[k] : 0;
+    const int o = k < n_nz ? nz_o[k] : 0;
+    const uint32_t word = k < n_nz ? bits[w] : 0u;
+    const bool dense = __popc(word) > kDenseBits;
+    unsigned m = __ballot_sync(0xffffffffu, dense);
+    while (m) {
+      const int src = __ffs(m) - 1;
+      m &= m - 1;
+      const uint32_t wd = __shfl_sync(0xffffffffu, word, src);
+      const int od = __shfl_sync(0xffffffffu, o, src);
+      const int wi = __shfl_sync(0xffffffffu, w, src);
+      if ((wd >> lane) & 1u) {
+        const int p = od + __popc(wd & lt);
+        if (p < W_max) out[p] = wi * 32 + lane;
+      }
+    }
+    if (!dense) {
+      uint32_t b = word;
+      int p = o;
+      while (b) {
+        const int i = __ffs(b) - 1;
+        b &= b - 1;
+        if (p < W_max) out[p] = w * 32 + i;
+        ++p;
+      }
+    }
   }
+  const int n = total < W_max ? total : W_max;
+  if (stage != nullptr) {
+    __syncthreads();
+    for (int j = tid; j < n; j += T) active[j] = stage[j];
+  }
+  if (tid == 0) {
+    if (total > W_max) set_flag(err, NS_FLAG_OVERFLOW);
+    *count = n;
+  }
+}
+
+// Dynamic shared memory of the state kernels, in words: the bitmap, the list
+// of nonzero words and their offsets, then (when W_max allows) the staged I_t.
+__host__ __device__ inline int state_smem_words(int nwords_pad, int W_max) {
+  return 3 * nwords_pad + (W_max <= kStageMaxW ? ((W_max + 3) & ~3) : 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -105,7 +201,6 @@ __global__ void init_reset_kernel(SeqDev s, Dims d) {
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     *s.length = 0;
     *s.count = 0;
-    *s.vticket = 0;
   }
 }
 
@@ -182,141 +277,450 @@ __global__ void __launch_bounds__(kStateThreads) init_compose_kernel(SeqDev s, D
 }
 
 // ---------------------------------------------------------------------------
-// Decode-step append (+ optional compaction)
+// Decode-step append (+ optional compaction): one cluster of 16 CTAs (8 where
+// the device cannot hold 16)
 // ---------------------------------------------------------------------------
-// All CTAs rank a slice of the verify row; the last CTA to finish merges the
-// slices into C_ver, builds C_draft, appends C_draft (+) C_ver to the ring,
-// updates counts and bitmap, and (BUILD) compacts the bitmap into I_t.
-template <int KMAX, bool VEC, bool BUILD>
-__global__ void __launch_bounds__(kStateThreads) append_kernel(SeqDev s, Dims d, const int32_t *tree, int n_tree,
-                                                               const float *zrow, uint32_t *err) {
-  __shared__ float sc_v[(kStateThreads / kWarp) * NS_MAX_SELECT_K];
-  __shared__ int sc_i[(kStateThreads / kWarp) * NS_MAX_SELECT_K];
-  __shared__ float res_v[NS_MAX_SELECT_K];
-  __shared__ int res_i[NS_MAX_SELECT_K];
+constexpr int kMaxStateCluster = 16;
+
+__device__ __forceinline__ uint32_t state_cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ int state_cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return (int)r;
+}
+__device__ __forceinline__ void state_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t leader_addr(const void *p) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)));
+  return r;
+}
+
+// Ranking order of a verify logit as an unsigned key: a larger key is a
+// larger value, so (key descending, id ascending) is the order of every
+// Top-K here.  NaN maps to 0, the key of an empty entry, and never ranks;
+// -0.0 takes the key of +0.0 so that the two tie.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  if (x != x) return 0u;
+  const uint32_t u = x == 0.f ? 0u : __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The best (key, id) held by the warp's lanes: the largest key, then the
+// smallest id.  An empty entry is (0, kEmptyId).
+__device__ __forceinline__ void warp_best(uint32_t k, uint32_t i, uint32_t &bk, uint32_t &bi) {
+  bk = __reduce_max_sync(0xffffffffu, k);
+  bi = __reduce_min_sync(0xffffffffu, k == bk ? i : 0xffffffffu);
+}
+
+// One warp: the K best entries of `nl` (<= 32) lists that are sorted best
+// first, K entries each (list l at lk/li[l * K]).  Lane l follows list l; each
+// round the best head wins and its list advances.  Winners go to ok/oi[r]
+// when ok is not null (outputs must not overlap the lists); every lane
+// returns the K-th winner in lastk/lasti.
+__device__ void warp_merge_lists(const uint32_t *lk, const uint32_t *li, int nl, int K, uint32_t *ok,
+                                 uint32_t *oi, uint32_t &lastk, uint32_t &lasti) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  int p = 0;
+  lastk = 0u;
+  lasti = (uint32_t)kEmptyId;
+  for (int r = 0; r < K; ++r) {
+    uint32_t hk = 0u, hi = (uint32_t)kEmptyId;
+    if (lane < nl && p < K) {
+      hk = lk[lane * K + p];
+      hi = li[lane * K + p];
+    }
+    uint32_t bk, bi;
+    warp_best(hk, hi, bk, bi);
+    if (ok != nullptr && lane == 0) {
+      ok[r] = bk;
+      oi[r] = bi;
+    }
+    if (bk != 0u && hk == bk && hi == bi) ++p;
+    lastk = bk;
+    lasti = bi;
+  }
+  __syncwarp();
+}
+
+// One warp: the K best of n unsorted entries at ck/ci (K rounds; each
+// round's winner is struck out in place).  Winners go to ok/oi[r].
+__device__ void warp_select_keys(uint32_t *ck, uint32_t *ci, int n, int K, uint32_t *ok, uint32_t *oi) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  for (int r = 0; r < K; ++r) {
+    uint32_t lk = 0u, li = (uint32_t)kEmptyId;
+    int lq = -1;
+    for (int q = lane; q < n; q += kWarp) {
+      const uint32_t k = ck[q], i = ci[q];
+      if (k > lk || (k == lk && k != 0u && i < li)) {
+        lk = k;
+        li = i;
+        lq = q;
+      }
+    }
+    uint32_t bk, bi;
+    warp_best(lk, li, bk, bi);
+    if (lane == 0) {
+      ok[r] = bk;
+      oi[r] = bi;
+    }
+    if (bk != 0u && lq >= 0 && lk == bk && li == bi) {
+      ck[lq] = 0u;
+      ci[lq] = (uint32_t)kEmptyId;
+    }
+    __syncwarp();
+  }
+}
+
+// The cluster's CTAs rank one slice each of the verify row and hand their Top-K
+// to the leader through distributed shared memory.  A CTA ranks its slice in
+// passes of 16 values per thread, held in registers: each thread takes the
+// best of its 16; the K-th best of those 1024 maxima is a threshold T that
+// every value of the pass's Top-K reaches, and only values at or above T (at
+// most K * 16: they all belong to the K threads whose maximum reaches T) are
+// collected and ranked exactly by one warp, together with the earlier passes'
+// Top-K.  Meanwhile the leader has pulled the tree ids, |S|, the ring slots
+// that can be evicted, their ids' window counts and (by a bulk copy) the
+// whole bitmap into shared memory, so after the cluster barrier it makes no
+// global round trip: the net change of every touched id's window count
+// (summed in a shared hash table) and the bitmap say which bits flip, and the
+// count and bitmap updates are fire-and-forget atomics.  It then rewrites the
+// ring and (BUILD) compacts the updated shared-memory bitmap into I_t.
+constexpr int kRankPer = 16;                           // verify values per thread per pass
+constexpr int kRankPass = kRankPer * kStateThreads;    // values per CTA per pass
+constexpr int kMaxCand = NS_MAX_SELECT_K * kRankPer;   // a pass's threshold candidates, at most
+constexpr int kStateWarps = kStateThreads / kWarp;
+constexpr int kHashSlots = 256;                        // >= the most distinct ids one step touches
+
+template <bool VEC, bool BUILD>
+__global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims d, const int32_t *tree, int n_tree, const float *zrow, uint32_t *err) {
+  extern __shared__ uint4 s_dyn4[];  // leader: the bitmap, the nonzero-word list (nwords_pad words each), the staged I_t
+  __shared__ uint32_t wl_k[kStateWarps * NS_MAX_SELECT_K], wl_i[kStateWarps * NS_MAX_SELECT_K];
+  __shared__ uint32_t cand_k[NS_MAX_SELECT_K + kMaxCand], cand_i[NS_MAX_SELECT_K + kMaxCand];
+  __shared__ uint32_t res_k[NS_MAX_SELECT_K], res_i[NS_MAX_SELECT_K];
+  __shared__ uint32_t cl_k[kMaxStateCluster * NS_MAX_SELECT_K], cl_i[kMaxStateCluster * NS_MAX_SELECT_K];
+  __shared__ uint32_t s_thr[2];
+  __shared__ int s_ncand;
   __shared__ int s_tree[NS_MAX_ROWS];
   __shared__ int s_app[kMaxAppend];
-  __shared__ int s_ev[kMaxAppend];
+  __shared__ int s_evict[kMaxAppend];
+  __shared__ uint32_t s_evc[kMaxAppend];
+  __shared__ int h_key[kHashSlots];
+  __shared__ int h_dl[kHashSlots];
+  __shared__ uint32_t h_old[kHashSlots];
   __shared__ int s_misc[4];
-  __shared__ int sh_scan[kStateThreads / kWarp];
+  __shared__ long long s_len;
+  __shared__ __align__(8) unsigned long long s_bar;  // the bitmap copy
+  __shared__ int sh_scan[2 * kWarp];
 
   const int tid = threadIdx.x;
+  const int warp = tid / kWarp, lane = tid & (kWarp - 1);
   const int K = d.K_ver;
+  const uint32_t rank = state_cluster_rank();
+  const int nct = state_cluster_size();
+  const bool leader = rank == 0;
+  uint32_t *s_bits = reinterpret_cast<uint32_t *>(s_dyn4);
+  int32_t *s_nzw = reinterpret_cast<int32_t *>(s_bits + d.nwords_pad);
+  int32_t *s_nzo = s_nzw + d.nwords_pad;
+  int32_t *s_stage = d.W_max <= kStageMaxW ? s_nzo + d.nwords_pad : nullptr;
 
-  // ---- C_ver = T_Kver(z_verify) -------------------------------------------
+  // ---- leader: the bitmap starts streaming into shared memory -------------
+  if (leader && tid == 0) {
+    mbar_init(smem_u32(&s_bar), 1);
+    mbar_fence_init();
+    mbar_expect_tx(smem_u32(&s_bar), (uint32_t)d.nwords_pad * 4);
+    bulk_load(smem_u32(s_bits), s.bitmap, (uint32_t)d.nwords_pad * 4, smem_u32(&s_bar));
+  }
+  // Distributed shared memory may only be written once every CTA of the
+  // cluster is running: arrive now, wait just before the first remote store.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
+  // ---- this CTA's slice of the verify row; the first pass's loads ----------
+  int lo = 0, nslice = 0;
   if (K > 0) {
-    TopList<KMAX> L;
-    L.clear();
-    const int gstride = gridDim.x * blockDim.x;
-    if (VEC) {
-      const int n4 = d.V >> 2;
-      for (int q = blockIdx.x * blockDim.x + tid; q < n4; q += gstride) {
-        const float4 f = __ldcs(reinterpret_cast<const float4 *>(zrow) + q);
-        L.insert(f.x, 4 * q);
-        L.insert(f.y, 4 * q + 1);
-        L.insert(f.z, 4 * q + 2);
-        L.insert(f.w, 4 * q + 3);
+    const int S = ((d.V / 4 + nct - 1) / nct) * 4;  // values per CTA, a multiple of 4
+    lo = (int)rank * S;
+    nslice = d.V - lo < S ? d.V - lo : S;
+    if (nslice < 0) nslice = 0;
+  }
+  float x[kRankPer];
+  auto load_pass = [&](int c0) {
+    const int n = nslice - c0 < kRankPass ? nslice - c0 : kRankPass;
+    if (VEC) {  // zrow is 16-byte aligned and lo, c0, n are multiples of 4
+      const float4 *z4 = reinterpret_cast<const float4 *>(zrow + lo + c0);
+#pragma unroll
+      for (int q = 0; q < kRankPer / 4; ++q) {
+        const int u = q * kStateThreads + tid;
+        float4 f = make_float4(__int_as_float(0x7fffffff), __int_as_float(0x7fffffff), __int_as_float(0x7fffffff),
+                               __int_as_float(0x7fffffff));
+        if (4 * u < n) f = __ldcs(z4 + u);
+        x[4 * q] = f.x;
+        x[4 * q + 1] = f.y;
+        x[4 * q + 2] = f.z;
+        x[4 * q + 3] = f.w;
       }
     } else {
-      for (int q = blockIdx.x * blockDim.x + tid; q < d.V; q += gstride) L.insert(__ldcs(zrow + q), q);
-    }
-    block_select<KMAX>(L, K, sc_v, sc_i, res_v, res_i);
-    if (gridDim.x > 1) {
-      if (tid < K) {
-        s.vpart_v[blockIdx.x * K + tid] = res_v[tid];
-        s.vpart_i[blockIdx.x * K + tid] = res_i[tid];
+#pragma unroll
+      for (int q = 0; q < kRankPer; ++q) {
+        const int u = q * kStateThreads + tid;
+        x[q] = u < n ? __ldcs(zrow + lo + c0 + u) : __int_as_float(0x7fffffff);
       }
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) s_misc[0] = (atomicAdd(s.vticket, 1) == (int)gridDim.x - 1);
-      __syncthreads();
-      if (!s_misc[0]) return;
-      __threadfence();
-      if (tid == 0) *s.vticket = 0;
-      L.clear();
-      for (int q = tid; q < (int)gridDim.x * K; q += blockDim.x) L.insert(__ldcg(s.vpart_v + q), __ldcg(s.vpart_i + q));
-      block_select<KMAX>(L, K, sc_v, sc_i, res_v, res_i);
+    }
+  };
+  // id of x[q] in the pass starting at c0 (ascending in q for each thread)
+  auto id_of = [&](int c0, int q) -> uint32_t {
+    return VEC ? (uint32_t)(lo + c0 + 4 * ((q >> 2) * kStateThreads + tid) + (q & 3))
+               : (uint32_t)(lo + c0 + q * kStateThreads + tid);
+  };
+  if (nslice > 0) load_pass(0);
+
+  // ---- leader prologue: |S|, the tree ids -----------------------------------
+  if (leader) {
+    if (tid == 0) s_len = *s.length;
+    if (tid < n_tree) s_tree[tid] = tree[tid];
+    for (int q = tid; q < kHashSlots; q += blockDim.x) {
+      h_key[q] = -1;
+      h_dl[q] = 0;
+    }
+  }
+  if (tid < K) {  // the running Top-K starts empty
+    res_k[tid] = 0u;
+    res_i[tid] = (uint32_t)kEmptyId;
+  }
+  __syncthreads();  // the leader's s_len and s_tree; its barrier is initialised
+
+  const long long W = d.W_max;
+  const long long len0 = s_len;
+  const long long old_start = len0 > W ? len0 - W : 0;
+  const int max_ev = (int)((n_tree + K) < W ? (n_tree + K) : W);  // no step evicts more
+  int ev_id = -1;
+  if (leader && tid < max_ev) ev_id = s.ring[(old_start + tid) % W];  // used after the ranking
+
+  // ---- rank the slice -------------------------------------------------------
+  for (int c0 = 0; c0 < nslice; c0 += kRankPass) {
+    if (c0 > 0) load_pass(c0);
+    uint32_t mk = 0u, mi = (uint32_t)kEmptyId;  // this thread's best
+#pragma unroll
+    for (int q = 0; q < kRankPer; ++q) {
+      const uint32_t k = order_key(x[q]);
+      if (k > mk) {  // ids ascend with q, so the first of equal keys stays
+        mk = k;
+        mi = id_of(c0, q);
+      }
+    }
+    for (int r = 0; r < K; ++r) {  // this warp's K best maxima, best first
+      uint32_t bk, bi;
+      warp_best(mk, mi, bk, bi);
+      if (lane == 0) {
+        wl_k[warp * K + r] = bk;
+        wl_i[warp * K + r] = bi;
+      }
+      if (mk == bk && mi == bi) {
+        mk = 0u;
+        mi = (uint32_t)kEmptyId;
+      }
+    }
+    if (tid == 0) s_ncand = K;  // entries [0, K) hold the earlier passes' Top-K
+    if (tid < K) {
+      cand_k[tid] = res_k[tid];
+      cand_i[tid] = res_i[tid];
+    }
+    __syncthreads();
+    if (warp == 0) {  // T = the K-th best of the CTA's maxima
+      uint32_t tk, ti;
+      warp_merge_lists(wl_k, wl_i, kStateWarps, K, nullptr, nullptr, tk, ti);
+      if (lane == 0) {
+        s_thr[0] = tk;
+        s_thr[1] = ti;
+      }
+    }
+    __syncthreads();
+    const uint32_t tk = s_thr[0], ti = s_thr[1];
+#pragma unroll
+    for (int q = 0; q < kRankPer; ++q) {
+      const uint32_t k = order_key(x[q]);
+      if (k != 0u && k >= tk) {
+        const uint32_t i = id_of(c0, q);
+        if (k > tk || i <= ti) {
+          const int slot = atomicAdd(&s_ncand, 1);
+          if (slot < NS_MAX_SELECT_K + kMaxCand) {
+            cand_k[slot] = k;
+            cand_i[slot] = i;
+          } else {  // cannot happen: at most K * kRankPer values reach T
+            set_flag(err, NS_FLAG_INTERNAL | (4u << 8));
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int n = s_ncand < NS_MAX_SELECT_K + kMaxCand ? s_ncand : NS_MAX_SELECT_K + kMaxCand;
+      warp_select_keys(cand_k, cand_i, n, K, res_k, res_i);
+    }
+    __syncthreads();  // res is complete; x, wl and cand may be reused
+  }
+
+  // ---- leader: C_draft (warp 1), evicted ids' counts -------------------------
+  if (leader && warp == 1) {
+    // C_draft: distinct valid tree ids in first-occurrence order.  Lane l
+    // holds nodes l and l + 32; invalid ids get keys that match nothing.
+    const int a = lane < n_tree ? s_tree[lane] : 0;
+    const int b = lane + 32 < n_tree ? s_tree[lane + 32] : 0;
+    const bool va = lane < n_tree && (unsigned)a < (unsigned)d.V;
+    const bool vb = lane + 32 < n_tree && (unsigned)b < (unsigned)d.V;
+    if ((lane < n_tree && !va) || (lane + 32 < n_tree && !vb)) set_flag(err, NS_FLAG_BAD_ID);
+    const int ka = va ? a : -1 - lane, kb = vb ? b : -33 - lane;
+    const unsigned ma = __match_any_sync(0xffffffffu, ka);
+    const unsigned mb = __match_any_sync(0xffffffffu, kb);
+    bool in_a = false;
+#pragma unroll
+    for (int j = 0; j < kWarp; ++j) in_a |= __shfl_sync(0xffffffffu, ka, j) == kb;
+    const bool keep_a = va && __ffs(ma) - 1 == lane;
+    const bool keep_b = vb && __ffs(mb) - 1 == lane && !in_a;
+    const unsigned ba = __ballot_sync(0xffffffffu, keep_a), bb = __ballot_sync(0xffffffffu, keep_b);
+    const unsigned lt = (1u << lane) - 1u;
+    if (keep_a) s_app[__popc(ba & lt)] = a;
+    if (keep_b) s_app[__popc(ba) + __popc(bb & lt)] = b;
+    if (lane == 0) s_misc[2] = __popc(ba) + __popc(bb);
+  }
+  uint32_t ev_cnt = 0u;
+  if (ev_id >= 0) {
+    if ((unsigned)ev_id >= (unsigned)d.V) {  // the ring only ever holds valid ids
+      set_flag(err, NS_FLAG_INTERNAL | (2u << 8));
+      ev_id = -1;
+    } else {
+      ev_cnt = s.counts[ev_id];  // used after the merge
     }
   }
 
-  // Only this CTA is left: let a programmatically launched successor start
-  // its prologue; it waits for this grid's results before reading them.
+  // ---- the CTAs' Top-K to the leader ---------------------------------------
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (K > 0 && warp == 0 && lane < K) {
+    const uint32_t ak = leader_addr(cl_k + rank * K + lane), ai = leader_addr(cl_i + rank * K + lane);
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ak), "r"(res_k[lane]) : "memory");
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ai), "r"(res_i[lane]) : "memory");
+  }
+  if (leader) {  // the leader publishes nothing here, so its arrival need not wait for its own loads
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  } else {
+    state_cluster_sync();
+    return;
+  }
+
+  if (K > 0 && warp == 0) {
+    uint32_t lk, li;
+    warp_merge_lists(cl_k, cl_i, nct, K, res_k, res_i, lk, li);
+  }
+  if (tid < max_ev) {
+    s_evict[tid] = ev_id;
+    s_evc[tid] = ev_cnt;
+  }
+  __syncthreads();
+  // Let a programmatically launched successor start its prologue; it waits
+  // for this grid's results before reading them.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // ---- C_draft: distinct valid tree ids in first-occurrence order ----------
-  if (tid < n_tree) s_tree[tid] = tree[tid];
-  __syncthreads();
-  const int warp = tid / kWarp, lane = tid & (kWarp - 1);
-  int keep = 0, x = 0;
-  if (tid < n_tree) {
-    x = s_tree[tid];
-    keep = (unsigned)x < (unsigned)d.V;
-    if (!keep) set_flag(err, NS_FLAG_BAD_ID);
-    for (int j = 0; j < tid && keep; ++j)
-      if (s_tree[j] == x) keep = 0;
-  }
-  unsigned ball = 0;
-  if (warp < 2) ball = __ballot_sync(0xffffffffu, keep);
-  if (warp == 0 && lane == 0) s_misc[1] = __popc(ball);
-  __syncthreads();
-  if (warp < 2) {
-    const int pos = __popc(ball & ((1u << lane) - 1u)) + (warp == 1 ? s_misc[1] : 0);
-    if (keep) s_app[pos] = x;
-    if (warp == 1 && lane == 0) s_misc[2] = s_misc[1] + __popc(ball);
-  }
-  __syncthreads();
   const int n_draft = s_misc[2];
   // C_ver: the ranked ids are best first; a row without enough orderable
   // (non-NaN) values leaves empty slots at the end, which are not appended.
   int n_ver = 0;
-  for (int q = 0; q < K; ++q) n_ver += res_i[q] != kEmptyId;
-  if (tid < n_ver) s_app[n_draft + tid] = res_i[tid];
+  for (int q = 0; q < K; ++q) n_ver += res_k[q] != 0u;
+  if (tid < n_ver) {
+    int y = (int)res_i[tid];
+    if ((unsigned)y >= (unsigned)d.V) {  // cannot happen for a well-formed merge
+      set_flag(err, NS_FLAG_INTERNAL | (1u << 8));
+      y = 0;
+    }
+    s_app[n_draft + tid] = y;
+  }
   if (tid == 0 && n_ver < K) set_flag(err, NS_FLAG_BAD_ID);
   const int m = n_draft + n_ver;
+  __syncthreads();  // C_ver is in s_app before anyone reads the appended entries
 
-  // ---- append to the ring, evict, update counts and bitmap ----------------
-  const long long W = d.W_max;
-  const long long len0 = *s.length;
+  // ---- window: what enters (+1), what leaves (-1), net per distinct id -----
   const long long len1 = len0 + m;
   const long long new_start = len1 > W ? len1 - W : 0;
-  const long long old_start = len0 > W ? len0 - W : 0;
   const long long ev_end = len0 < new_start ? len0 : new_start;
   const int n_ev = ev_end > old_start ? (int)(ev_end - old_start) : 0;
   const long long ap_begin = len0 > new_start ? len0 : new_start;
   const int n_ap = (int)(len1 - ap_begin);
-  if (tid < n_ev) s_ev[tid] = s.ring[(old_start + tid) % W];
-  __syncthreads();
+  if (tid < n_ap + n_ev) {
+    int id, dl;
+    uint32_t old = 0u;
+    if (tid < n_ap) {
+      id = s_app[ap_begin + tid - len0];
+      dl = 1;
+    } else {
+      id = s_evict[tid - n_ap];
+      old = s_evc[tid - n_ap];
+      dl = -1;
+    }
+    if (id >= 0) {
+      unsigned slot = ((unsigned)id * 2654435761u) >> 24;  // 8-bit hash
+      for (int probe = 0; probe < kHashSlots; ++probe, slot = (slot + 1) & (kHashSlots - 1)) {
+        const int prev = atomicCAS(&h_key[slot], -1, id);
+        if (prev == -1 || prev == id) {
+          atomicAdd(&h_dl[slot], dl);
+          if (dl < 0) h_old[slot] = old;  // every eviction of an id read the same count
+          break;
+        }
+      }
+    }
+  }
   if (tid < n_ap) {
     const long long p = ap_begin + tid;
-    const int y = s_app[p - len0];
-    s.ring[p % W] = y;
-    atomicAdd(&s.counts[y], 1u);
+    s.ring[p % W] = s_app[p - len0];
   }
-  if (tid >= 128 && tid - 128 < n_ev) {
-    const unsigned old = atomicSub(&s.counts[s_ev[tid - 128]], 1u);
-    if (old == 0u) set_flag(err, NS_FLAG_OVERFLOW);
-  }
-  __threadfence();
-  __syncthreads();
-  int fix = -1;
-  if (tid < n_ap) fix = s_app[ap_begin + tid - len0];
-  else if (tid >= 128 && tid - 128 < n_ev) fix = s_ev[tid - 128];
-  if (fix >= 0) {
-    const unsigned c = atomicAdd(&s.counts[fix], 0u);
-    const unsigned bit = 1u << (fix & 31);
-    if (c) atomicOr(&s.bitmap[fix >> 5], bit);
-    else atomicAnd(&s.bitmap[fix >> 5], ~bit);
-  }
-  __threadfence();
-  __syncthreads();
   if (tid == 0) *s.length = len1;
+  // The bitmap copy must have landed before its bits are read.  If the wait
+  // gave up (NS_FLAG_TIMEOUT), the bitmap and I_t are left as they were.
+  const bool have_bits = __syncthreads_and(mbar_wait(smem_u32(&s_bar), 0, err));
+  // One thread per distinct id.  A net gain sets the bit of an id that was
+  // outside the window (bit clear: count 0); a net loss happens only to an
+  // evicted id, whose count was read above, and clears the bit when the
+  // count reaches 0.
+  if (tid < kHashSlots) {
+    const int id = h_key[tid], net = h_dl[tid];
+    if (id >= 0 && net != 0) {
+      atomicAdd(&s.counts[id], (unsigned)net);
+      const unsigned bit = 1u << (id & 31);
+      if (net > 0) {
+        if (have_bits && !(s_bits[id >> 5] & bit)) {
+          atomicOr(&s_bits[id >> 5], bit);
+          atomicOr(&s.bitmap[id >> 5], bit);
+        }
+      } else {
+        const long long now = (long long)h_old[tid] + net;
+        if (now < 0) set_flag(err, NS_FLAG_OVERFLOW);
+        if (now == 0 && have_bits) {
+          atomicAnd(&s_bits[id >> 5], ~bit);
+          atomicAnd(&s.bitmap[id >> 5], ~bit);
+        }
+      }
+    }
+  }
+  __syncthreads();
 
-  if (BUILD) compact_bitmap(s.bitmap, d.nwords_pad, s.active, s.count, d.W_max, err, sh_scan);
+  if (BUILD && have_bits)
+    compact_bitmap(s_bits, d.nwords, d.nwords_pad, s_nzw, s_nzo, s_stage, s.active, s.count, d.W_max, err, sh_scan);
 }
 
 __global__ void __launch_bounds__(kStateThreads) build_kernel(SeqDev s, Dims d, uint32_t *err) {
-  __shared__ int sh_scan[kStateThreads / kWarp];
-  compact_bitmap(s.bitmap, d.nwords_pad, s.active, s.count, d.W_max, err, sh_scan);
+  extern __shared__ uint4 s_dyn4[];  // the bitmap, the nonzero-word list (nwords_pad words each), the staged I_t
+  __shared__ int sh_scan[2 * kWarp];
+  uint32_t *s_bits = reinterpret_cast<uint32_t *>(s_dyn4);
+  int32_t *s_nzw = reinterpret_cast<int32_t *>(s_bits + d.nwords_pad);
+  int32_t *s_nzo = s_nzw + d.nwords_pad;
+  int32_t *s_stage = d.W_max <= kStageMaxW ? s_nzo + d.nwords_pad : nullptr;
+  const uint4 *g4 = reinterpret_cast<const uint4 *>(s.bitmap);
+  for (int q = threadIdx.x; q < d.nwords_pad / 4; q += blockDim.x) s_dyn4[q] = g4[q];
+  __syncthreads();
+  compact_bitmap(s_bits, d.nwords, d.nwords_pad, s_nzw, s_nzo, s_stage, s.active, s.count, d.W_max, err, sh_scan);
 }
 
 // packed[j, :] = W[I_t[j], :]; each CTA copies 4 rows per iteration with all
@@ -364,13 +768,51 @@ cudaError_t launch_prefill_topk(const SeqDev &s, const Dims &d, const float *Z, 
 }
 
 template <bool VEC, bool BUILD>
-cudaError_t launch_append_k(const SeqDev &s, const Dims &d, int vgrid, const int32_t *tree, int n_tree,
-                            const float *zrow, uint32_t *err, cudaStream_t st) {
-  const int K = d.K_ver;
-  if (K <= 4) append_kernel<4, VEC, BUILD><<<vgrid, kStateThreads, 0, st>>>(s, d, tree, n_tree, zrow, err);
-  else if (K <= 8) append_kernel<8, VEC, BUILD><<<vgrid, kStateThreads, 0, st>>>(s, d, tree, n_tree, zrow, err);
-  else append_kernel<16, VEC, BUILD><<<vgrid, kStateThreads, 0, st>>>(s, d, tree, n_tree, zrow, err);
-  return cudaGetLastError();
+cudaError_t launch_append_k(const SeqDev &s, const Dims &d, const int32_t *tree, int n_tree, const float *zrow,
+                            uint32_t *err, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(d.state_cluster, 1, 1);
+  cfg.blockDim = dim3(kStateThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)state_smem_words(d.nwords_pad, d.W_max) * 4;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = d.state_cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, append_kernel<VEC, BUILD>, s, d, tree, n_tree, zrow, err);
+}
+
+template <bool VEC, bool BUILD>
+cudaError_t allow_append(int bytes) {
+  cudaError_t e = cudaFuncSetAttribute(append_kernel<VEC, BUILD>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(append_kernel<VEC, BUILD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+// Whether a cluster of `n` append CTAs with `bytes` of dynamic shared memory
+// can be resident on this device.
+bool cluster_fits(int n, int bytes) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n, 1, 1);
+  cfg.blockDim = dim3(kStateThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)bytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = n;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, append_kernel<true, true>, &cfg);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return clusters >= 1;
 }
 
 }  // namespace
@@ -403,20 +845,32 @@ cudaError_t launch_init(const SeqDev &s, const Dims &d, const int32_t *prompt, i
   return cudaGetLastError();
 }
 
-cudaError_t launch_append(const SeqDev &s, const Dims &d, int vgrid, const int32_t *tree, int n_tree,
-                          const float *zrow, bool build, uint32_t *err, cudaStream_t st) {
+cudaError_t prepare_state_kernels(Dims *d) {
+  const int bytes = state_smem_words(d->nwords_pad, d->W_max) * 4;
+  cudaError_t e = cudaSuccess;
+  const cudaError_t r[] = {allow_append<true, true>(bytes), allow_append<true, false>(bytes),
+                           allow_append<false, true>(bytes), allow_append<false, false>(bytes),
+                           cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)};
+  for (cudaError_t x : r)
+    if (x != cudaSuccess) e = x;
+  if (e != cudaSuccess) return e;
+  d->state_cluster = cluster_fits(kMaxStateCluster, bytes) ? kMaxStateCluster : 8;
+  return cluster_fits(d->state_cluster, bytes) ? cudaSuccess : cudaErrorNotSupported;
+}
+
+cudaError_t launch_append(const SeqDev &s, const Dims &d, const int32_t *tree, int n_tree, const float *zrow,
+                          bool build, uint32_t *err, cudaStream_t st) {
   const bool vec = d.K_ver > 0 && (d.V % 4 == 0) && (reinterpret_cast<uintptr_t>(zrow) % 16 == 0);
-  const int grid = d.K_ver > 0 ? vgrid : 1;
   if (vec) {
-    return build ? launch_append_k<true, true>(s, d, grid, tree, n_tree, zrow, err, st)
-                 : launch_append_k<true, false>(s, d, grid, tree, n_tree, zrow, err, st);
+    return build ? launch_append_k<true, true>(s, d, tree, n_tree, zrow, err, st)
+                 : launch_append_k<true, false>(s, d, tree, n_tree, zrow, err, st);
   }
-  return build ? launch_append_k<false, true>(s, d, grid, tree, n_tree, zrow, err, st)
-               : launch_append_k<false, false>(s, d, grid, tree, n_tree, zrow, err, st);
+  return build ? launch_append_k<false, true>(s, d, tree, n_tree, zrow, err, st)
+               : launch_append_k<false, false>(s, d, tree, n_tree, zrow, err, st);
 }
 
 cudaError_t launch_build(const SeqDev &s, const Dims &d, uint32_t *err, cudaStream_t st) {
-  build_kernel<<<1, kStateThreads, 0, st>>>(s, d, err);
+  build_kernel<<<1, kStateThreads, (size_t)state_smem_words(d.nwords_pad, d.W_max) * 4, st>>>(s, d, err);
   return cudaGetLastError();
 }
 

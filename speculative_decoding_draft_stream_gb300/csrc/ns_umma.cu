@@ -37,6 +37,7 @@
 #include <mutex>
 
 #include "ns_internal.cuh"
+#include "ns_ptx.cuh"
 
 namespace ns {
 namespace {
@@ -64,7 +65,6 @@ constexpr int kPartBytes = kUN * kUM * 4;    // one CTA's partial tile, [r][j] f
 constexpr int kMiscBytes = 1024;             // barriers, TMEM slot, ticket flag, row ids
 constexpr int kUSmem = kRingBytes + kMiscBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 64;
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
 
 static_assert(kPartBytes + kSlice * kUM * 4 + 2 * kSlice * NS_MAX_TOPK * 4 <= kRingBytes,
               "epilogue buffers reuse the stage ring");
@@ -72,44 +72,6 @@ static_assert(kPartBytes + kSlice * kUM * 4 + 2 * kSlice * NS_MAX_TOPK * 4 <= kR
 // D = fp32, A = B = bf16, both K-major, N = 64, M = 128.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kUN >> 3) << 17) |
                             ((uint32_t)(kUM >> 4) << 24);
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// ---- mbarrier ---------------------------------------------------------------
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait on a phase; false (and NS_FLAG_TIMEOUT) when it runs out.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) {
-      atomicOr(err, NS_FLAG_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
 
 // ---- TMA ------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap *m) {
@@ -209,7 +171,7 @@ struct UmmaArgs {
   const uint16_t *W;         // W_head [V x H]
   const int32_t *idx;        // I_t ascending
   const int32_t *count_ptr;  // |I_t|
-  int32_t H, n, k;
+  int32_t V, H, n, k;
   float *logits;             // [n x ld]
   int32_t ld;
   float *cand_v;             // [tiles x 64 x k] per-tile candidates
@@ -248,7 +210,7 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
       mbar_init(bar_empty + 8 * s, 2);                  // the MMA commit and the packed-store issuer
     }
     mbar_init(bar_acc, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_fence_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
@@ -278,7 +240,12 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
   const int row0 = tile * kUM;
   if (tid < kUM) {
     const int j = row0 + tid;
-    s_rows[tid] = a.idx[j < m ? j : m - 1];  // rows past |I_t| repeat the last active row
+    int id = a.idx[j < m ? j : m - 1];  // rows past |I_t| repeat the last active row
+    if ((unsigned)id >= (unsigned)a.V) {  // I_t only holds valid ids
+      atomicOr(a.err, NS_FLAG_INTERNAL | (3u << 8));
+      id = 0;
+    }
+    s_rows[tid] = id;
   }
   __syncthreads();
 
@@ -522,6 +489,7 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   a.W = L.W;
   a.idx = L.idx;
   a.count_ptr = L.count_ptr;
+  a.V = L.V;
   a.H = L.H;
   a.n = L.n;
   a.k = L.k;

@@ -23,6 +23,7 @@ STATUS_NAMES = {0: "NS_OK", -1: "NS_ERR_ARG", -2: "NS_ERR_CUDA", -3: "NS_ERR_OOM
 FLAG_BAD_ID = 0x1
 FLAG_OVERFLOW = 0x2
 FLAG_TIMEOUT = 0x4
+FLAG_INTERNAL = 0x8
 MAX_SELECT_K = 16
 MAX_TOPK = 32
 MAX_ROWS = 64
