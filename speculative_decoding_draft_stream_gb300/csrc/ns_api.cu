@@ -74,8 +74,8 @@ void layout(ns_handle *h, Carver &cv) {
     s.cand = c.K_pre > 0 ? cv.take<int32_t>((size_t)c.max_prompt * c.K_pre) : nullptr;
     s.sinit = cv.take<int32_t>((size_t)c.max_prompt * (1 + c.K_pre));
     const size_t ncand = (size_t)ns::umma_tiles(c.W_max) * ns::kProjBN * c.max_k;
-    s.cand_v = cv.take<float>(ncand);
-    s.cand_i = cv.take<int32_t>(ncand);
+    s.cand_k = cv.take<uint32_t>(ncand);
+    s.cand_i = cv.take<uint32_t>(ncand);
     s.slice_ticket = cv.take<int32_t>(ns::umma_cluster());
   }
   h->dense_ld = (c.V + 3) & ~3;
@@ -297,7 +297,7 @@ static cudaError_t enqueue_gather_project(ns_handle *h, int32_t seq, const uint1
   L.k = k;
   L.logits = d_logits ? d_logits : s.logits;
   L.ld = d_logits ? ld_logits : h->dims.ld_scratch;
-  L.cand_v = s.cand_v;
+  L.cand_k = s.cand_k;
   L.cand_i = s.cand_i;
   L.slice_ticket = s.slice_ticket;
   L.out_ids = d_ids;

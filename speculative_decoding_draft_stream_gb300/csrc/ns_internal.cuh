@@ -38,8 +38,8 @@ struct SeqDev {
   int32_t *first;     // [V] first flat index of an id in the prefill union (init only)
   int32_t *cand;      // [max_prompt x K_pre] prefill Top-K ids (init only)
   int32_t *sinit;     // [max_prompt x (1 + K_pre)] S_init entries (init only)
-  float *cand_v;      // [umma tiles x 64 x max_k] per-tile top-k candidates
-  int32_t *cand_i;
+  uint32_t *cand_k;   // [umma tiles x 64 x max_k] per-tile top-k candidates (order keys)
+  uint32_t *cand_i;
   int32_t *slice_ticket;  // [umma cluster] arrival counters of the row slices
 };
 
@@ -146,59 +146,130 @@ __device__ void block_select(TopList<KMAX> &L, int K, float *sc_v, int *sc_i, fl
   __syncthreads();
 }
 
-// Warp-wide streaming Top-K (K <= 32).  Lane q < K holds the q-th best value
-// pushed so far (larger value first, then smaller id); (tv, ti) is the K-th
-// best, uniform across the warp.  Each push hands one value per lane; a value
-// costs a compare and a vote unless it beats the K-th best, which is rare, and
-// only then is it merged into the lane-distributed list.
-struct WarpStreamTopK {
-  float lv, tv;
-  int li, ti, K;
-  __device__ __forceinline__ void init(int k) {
-    K = k;
-    lv = tv = -__int_as_float(0x7f800000);
-    li = ti = kEmptyId;
-  }
-  __device__ __forceinline__ void push(float x, int i) {
-    const int lane = threadIdx.x & (kWarp - 1);
-    unsigned m = __ballot_sync(0xffffffffu, better(x, i, tv, ti));
-    while (m) {
-      const int src = __ffs(m) - 1;
-      m &= m - 1;
-      const float cx = __shfl_sync(0xffffffffu, x, src);
-      const int ci = __shfl_sync(0xffffffffu, i, src);
-      if (!better(cx, ci, tv, ti)) continue;  // the threshold rose since the vote
-      const int pos = __popc(__ballot_sync(0xffffffffu, lane < K && better(lv, li, cx, ci)));
-      const float uv = __shfl_up_sync(0xffffffffu, lv, 1);
-      const int ui = __shfl_up_sync(0xffffffffu, li, 1);
-      if (lane < K && lane > pos) {
-        lv = uv;
-        li = ui;
-      } else if (lane == pos) {
-        lv = cx;
-        li = ci;
-      }
-      tv = __shfl_sync(0xffffffffu, lv, K - 1);
-      ti = __shfl_sync(0xffffffffu, li, K - 1);
-    }
-  }
-};
+// Ranking order of a float as an unsigned key: a larger key is a larger
+// value, so (key descending, id ascending) is the Top-K order of `better`.
+// NaN maps to 0, the key of an empty entry, and never ranks; -0.0 takes the
+// key of +0.0 so that the two tie.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  if (x != x) return 0u;
+  const uint32_t u = x == 0.f ? 0u : __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// The value of a nonzero key (+0.0 for a key that came from -0.0).
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
 
-// Sorts one (value, id) per lane across the warp, best first (bitonic network).
-__device__ __forceinline__ void warp_sort_desc(float &v, int &i) {
+// The best (key, id) held by the warp's lanes: the largest key, then the
+// smallest id.  An empty entry is (0, kEmptyId).
+__device__ __forceinline__ void warp_best(uint32_t k, uint32_t i, uint32_t &bk, uint32_t &bi) {
+  bk = __reduce_max_sync(0xffffffffu, k);
+  bi = __reduce_min_sync(0xffffffffu, k == bk ? i : 0xffffffffu);
+}
+
+// One warp: the K best entries of `nl` (<= 32) lists that are sorted best
+// first, K entries each (list l at lk/li[l * K]).  Lane l follows list l; each
+// round the best head wins and its list advances.  Winners go to ok/oi[r]
+// when ok is not null (outputs must not overlap the lists); every lane
+// returns the K-th winner in lastk/lasti.
+__device__ __forceinline__ void warp_merge_lists(const uint32_t *lk, const uint32_t *li, int nl, int K,
+                                                 uint32_t *ok, uint32_t *oi, uint32_t &lastk, uint32_t &lasti) {
   const int lane = threadIdx.x & (kWarp - 1);
-#pragma unroll
-  for (int k = 2; k <= kWarp; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, v, j);
-      const int oi = __shfl_xor_sync(0xffffffffu, i, j);
-      const bool take_better = ((lane & j) == 0) == ((lane & k) == 0);
-      if (take_better ? better(ov, oi, v, i) : better(v, i, ov, oi)) {
-        v = ov;
-        i = oi;
+  int p = 0;
+  lastk = 0u;
+  lasti = (uint32_t)kEmptyId;
+  for (int r = 0; r < K; ++r) {
+    uint32_t hk = 0u, hi = (uint32_t)kEmptyId;
+    if (lane < nl && p < K) {
+      hk = lk[lane * K + p];
+      hi = li[lane * K + p];
+    }
+    uint32_t bk, bi;
+    warp_best(hk, hi, bk, bi);
+    if (ok != nullptr && lane == 0) {
+      ok[r] = bk;
+      oi[r] = bi;
+    }
+    if (bk != 0u && hk == bk && hi == bi) ++p;
+    lastk = bk;
+    lasti = bi;
+  }
+  __syncwarp();
+}
+
+// Sorts four (key, id) pairs best first (key descending, then id ascending).
+__device__ __forceinline__ void sort4_desc(uint32_t *k, uint32_t *i) {
+  auto cs = [&](int x, int y) {
+    if (k[y] > k[x] || (k[y] == k[x] && i[y] < i[x])) {
+      const uint32_t tk = k[x], ti = i[x];
+      k[x] = k[y];
+      i[x] = i[y];
+      k[y] = tk;
+      i[y] = ti;
+    }
+  };
+  cs(0, 1);
+  cs(2, 3);
+  cs(0, 2);
+  cs(1, 3);
+  cs(1, 2);
+}
+
+// One warp: the K best of four (key, id) pairs per lane, held in registers:
+// each lane sorts its four, then K rounds of a warp-wide best-of-heads, the
+// winner's lane moving to its next entry.  Lane 0 writes winner r to ok/oi[r]
+// (global or shared).
+__device__ __forceinline__ void warp_topk4(uint32_t *hk, uint32_t *hi, int K, uint32_t *ok, uint32_t *oi) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  sort4_desc(hk, hi);
+  for (int r = 0; r < K; ++r) {
+    uint32_t bk, bi;
+    warp_best(hk[0], hi[0], bk, bi);
+    if (lane == 0) {
+      ok[r] = bk;
+      oi[r] = bi;
+    }
+    if (bk != 0u && hk[0] == bk && hi[0] == bi) {
+      hk[0] = hk[1];
+      hi[0] = hi[1];
+      hk[1] = hk[2];
+      hi[1] = hi[2];
+      hk[2] = hk[3];
+      hi[2] = hi[3];
+      hk[3] = 0u;
+      hi[3] = (uint32_t)kEmptyId;
+    }
+  }
+  __syncwarp();
+}
+
+// One warp: the K best of n unsorted entries at ck/ci (K rounds; each
+// round's winner is struck out in place).  Winners go to ok/oi[r].
+__device__ __forceinline__ void warp_select_keys(uint32_t *ck, uint32_t *ci, int n, int K, uint32_t *ok,
+                                                 uint32_t *oi) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  for (int r = 0; r < K; ++r) {
+    uint32_t lk = 0u, li = (uint32_t)kEmptyId;
+    int lq = -1;
+    for (int q = lane; q < n; q += kWarp) {
+      const uint32_t k = ck[q], i = ci[q];
+      if (k > lk || (k == lk && k != 0u && i < li)) {
+        lk = k;
+        li = i;
+        lq = q;
       }
     }
+    uint32_t bk, bi;
+    warp_best(lk, li, bk, bi);
+    if (lane == 0) {
+      ok[r] = bk;
+      oi[r] = bi;
+    }
+    if (bk != 0u && lq >= 0 && lk == bk && li == bi) {
+      ck[lq] = 0u;
+      ci[lq] = (uint32_t)kEmptyId;
+    }
+    __syncwarp();
   }
 }
 
@@ -253,8 +324,8 @@ struct UmmaLaunch {
   int32_t k;
   float *logits;             // [n x ld]
   int32_t ld;
-  float *cand_v;             // [umma_tiles(W_max) x 64 x k]
-  int32_t *cand_i;
+  uint32_t *cand_k;          // [umma_tiles(W_max) x 64 x k]
+  uint32_t *cand_i;
   int32_t *slice_ticket;     // [umma_cluster()]
   int32_t *out_ids;          // [n x k]
   float *out_vals;

@@ -301,82 +301,6 @@ __device__ __forceinline__ uint32_t leader_addr(const void *p) {
   return r;
 }
 
-// Ranking order of a verify logit as an unsigned key: a larger key is a
-// larger value, so (key descending, id ascending) is the order of every
-// Top-K here.  NaN maps to 0, the key of an empty entry, and never ranks;
-// -0.0 takes the key of +0.0 so that the two tie.
-__device__ __forceinline__ uint32_t order_key(float x) {
-  if (x != x) return 0u;
-  const uint32_t u = x == 0.f ? 0u : __float_as_uint(x);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// The best (key, id) held by the warp's lanes: the largest key, then the
-// smallest id.  An empty entry is (0, kEmptyId).
-__device__ __forceinline__ void warp_best(uint32_t k, uint32_t i, uint32_t &bk, uint32_t &bi) {
-  bk = __reduce_max_sync(0xffffffffu, k);
-  bi = __reduce_min_sync(0xffffffffu, k == bk ? i : 0xffffffffu);
-}
-
-// One warp: the K best entries of `nl` (<= 32) lists that are sorted best
-// first, K entries each (list l at lk/li[l * K]).  Lane l follows list l; each
-// round the best head wins and its list advances.  Winners go to ok/oi[r]
-// when ok is not null (outputs must not overlap the lists); every lane
-// returns the K-th winner in lastk/lasti.
-__device__ void warp_merge_lists(const uint32_t *lk, const uint32_t *li, int nl, int K, uint32_t *ok,
-                                 uint32_t *oi, uint32_t &lastk, uint32_t &lasti) {
-  const int lane = threadIdx.x & (kWarp - 1);
-  int p = 0;
-  lastk = 0u;
-  lasti = (uint32_t)kEmptyId;
-  for (int r = 0; r < K; ++r) {
-    uint32_t hk = 0u, hi = (uint32_t)kEmptyId;
-    if (lane < nl && p < K) {
-      hk = lk[lane * K + p];
-      hi = li[lane * K + p];
-    }
-    uint32_t bk, bi;
-    warp_best(hk, hi, bk, bi);
-    if (ok != nullptr && lane == 0) {
-      ok[r] = bk;
-      oi[r] = bi;
-    }
-    if (bk != 0u && hk == bk && hi == bi) ++p;
-    lastk = bk;
-    lasti = bi;
-  }
-  __syncwarp();
-}
-
-// One warp: the K best of n unsorted entries at ck/ci (K rounds; each
-// round's winner is struck out in place).  Winners go to ok/oi[r].
-__device__ void warp_select_keys(uint32_t *ck, uint32_t *ci, int n, int K, uint32_t *ok, uint32_t *oi) {
-  const int lane = threadIdx.x & (kWarp - 1);
-  for (int r = 0; r < K; ++r) {
-    uint32_t lk = 0u, li = (uint32_t)kEmptyId;
-    int lq = -1;
-    for (int q = lane; q < n; q += kWarp) {
-      const uint32_t k = ck[q], i = ci[q];
-      if (k > lk || (k == lk && k != 0u && i < li)) {
-        lk = k;
-        li = i;
-        lq = q;
-      }
-    }
-    uint32_t bk, bi;
-    warp_best(lk, li, bk, bi);
-    if (lane == 0) {
-      ok[r] = bk;
-      oi[r] = bi;
-    }
-    if (bk != 0u && lq >= 0 && lk == bk && li == bi) {
-      ck[lq] = 0u;
-      ci[lq] = (uint32_t)kEmptyId;
-    }
-    __syncwarp();
-  }
-}
-
 // The cluster's CTAs rank one slice each of the verify row and hand their Top-K
 // to the leader through distributed shared memory.  A CTA ranks its slice in
 // passes of 16 values per thread, held in registers: each thread takes the
@@ -504,14 +428,29 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
   // ---- rank the slice -------------------------------------------------------
   for (int c0 = 0; c0 < nslice; c0 += kRankPass) {
     if (c0 > 0) load_pass(c0);
-    uint32_t mk = 0u, mi = (uint32_t)kEmptyId;  // this thread's best
+    // this thread's best, compared as floats (NaN never wins; -0.0 ties
+    // +0.0); ids ascend with q, so the first of equal values stays
+    float mv = -__int_as_float(0x7f800000);
+    int mq = -1;
 #pragma unroll
     for (int q = 0; q < kRankPer; ++q) {
-      const uint32_t k = order_key(x[q]);
-      if (k > mk) {  // ids ascend with q, so the first of equal keys stays
-        mk = k;
-        mi = id_of(c0, q);
+      if (x[q] > mv) {
+        mv = x[q];
+        mq = q;
       }
+    }
+    if (mq < 0) {  // nothing above -inf: the first -inf, if any
+      for (int q = 0; q < kRankPer; ++q) {
+        if (x[q] == mv) {
+          mq = q;
+          break;
+        }
+      }
+    }
+    uint32_t mk = 0u, mi = (uint32_t)kEmptyId;
+    if (mq >= 0) {
+      mk = order_key(mv);
+      mi = id_of(c0, mq);
     }
     for (int r = 0; r < K; ++r) {  // this warp's K best maxima, best first
       uint32_t bk, bi;
@@ -541,12 +480,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
     }
     __syncthreads();
     const uint32_t tk = s_thr[0], ti = s_thr[1];
+    const float tv = tk != 0u ? key_value(tk) : -__int_as_float(0x7f800000);
 #pragma unroll
     for (int q = 0; q < kRankPer; ++q) {
-      const uint32_t k = order_key(x[q]);
-      if (k != 0u && k >= tk) {
-        const uint32_t i = id_of(c0, q);
-        if (k > tk || i <= ti) {
+      if (x[q] >= tv) {  // rare: the exact test in key order
+        const uint32_t k = order_key(x[q]), i = id_of(c0, q);
+        if (k != 0u && (k > tk || (k == tk && i <= ti))) {
           const int slot = atomicAdd(&s_ncand, 1);
           if (slot < NS_MAX_SELECT_K + kMaxCand) {
             cand_k[slot] = k;
@@ -560,7 +499,18 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
     __syncthreads();
     if (warp == 0) {
       const int n = s_ncand < NS_MAX_SELECT_K + kMaxCand ? s_ncand : NS_MAX_SELECT_K + kMaxCand;
-      warp_select_keys(cand_k, cand_i, n, K, res_k, res_i);
+      if (n <= 4 * kWarp) {  // the usual case: a few candidates, ranked from registers
+        uint32_t hk[4], hi[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = lane + q * kWarp;
+          hk[q] = e < n ? cand_k[e] : 0u;
+          hi[q] = e < n ? cand_i[e] : (uint32_t)kEmptyId;
+        }
+        warp_topk4(hk, hi, K, res_k, res_i);
+      } else {
+        warp_select_keys(cand_k, cand_i, n, K, res_k, res_i);
+      }
     }
     __syncthreads();  // res is complete; x, wl and cand may be reused
   }

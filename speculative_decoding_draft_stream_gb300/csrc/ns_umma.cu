@@ -25,8 +25,8 @@
 // barrier CTA c adds the eight partials for hidden rows [8c, 8c+8) through
 // distributed shared memory in a fixed order (deterministic), ranks each
 // row's 128 columns (one warp per row) and writes those logits.  The
-// per-tile candidates of a row slice are merged by the last CTA of that slice
-// to finish (atomic ticket) into the final top-k.
+// per-tile candidates (sorted) of a row slice are merged by the last CTA of
+// that slice to finish (release/acquire ticket) into the final top-k.
 //
 // Every wait is bounded (about a second); a wait that runs out sets
 // NS_FLAG_TIMEOUT and the kernel still follows the same barrier sequence and
@@ -66,7 +66,10 @@ constexpr int kMiscBytes = 1024;             // barriers, TMEM slot, ticket flag
 constexpr int kUSmem = kRingBytes + kMiscBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 64;
 
-static_assert(kPartBytes + kSlice * kUM * 4 + 2 * kSlice * NS_MAX_TOPK * 4 <= kRingBytes,
+constexpr int kMergeLists = 24;  // tiles' lists merged per round of the final merge (+ the running list)
+constexpr int kMergeWarpWords = (kMergeLists + 1) * NS_MAX_TOPK;
+constexpr int kMergeBatch = 8;   // candidate loads a lane keeps in flight while staging
+static_assert(kPartBytes + kSlice * kUM * 4 + kSlice * (2 * kMergeWarpWords + 2 * NS_MAX_TOPK) * 4 <= kRingBytes,
               "epilogue buffers reuse the stage ring");
 
 // D = fp32, A = B = bf16, both K-major, N = 64, M = 128.
@@ -174,15 +177,14 @@ struct UmmaArgs {
   int32_t V, H, n, k;
   float *logits;             // [n x ld]
   int32_t ld;
-  float *cand_v;             // [tiles x 64 x k] per-tile candidates
-  int32_t *cand_i;
+  uint32_t *cand_k;          // [tiles x 64 x k] per-tile candidates: order keys, best first
+  uint32_t *cand_i;          // and their ids
   int32_t *slice_ticket;     // [kUCluster]
   int32_t *out_ids;          // [n x k]
   float *out_vals;
   uint32_t *err;
 };
 
-template <int KMAX>
 __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1)
     umma_step_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmP,
                      UmmaArgs a) {
@@ -370,24 +372,26 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
   __syncthreads();
 
   // ---- per-tile top-k of each row (one warp per hidden row) -----------------
-  // Candidates carry global ids (I_t is ascending, so id order = column order).
+  // Each lane sorts its four columns (value descending, then id ascending; I_t
+  // is ascending, so ids ascend with the column), and k rounds of a warp-wide
+  // best-of-heads write the tile's k best, best first, with global ids.
   const int r = (int)crank * kSlice + warp;
   if (r < a.n) {
-    TopList<4> L;
-    L.clear();
+    uint32_t hk[4], hi[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int j = lane + 32 * q;
-      if (row0 + j < m) L.insert(F[warp * kUM + j], s_rows[j]);
+      hk[q] = row0 + j < m ? order_key(F[warp * kUM + j]) : 0u;
+      hi[q] = hk[q] != 0u ? (uint32_t)s_rows[j] : (uint32_t)kEmptyId;
     }
     const size_t o = ((size_t)tile * kUN + r) * a.k;
-    warp_select<4>(L, a.k, a.cand_v + o, a.cand_i + o);
-    if (lane == 0) __threadfence();  // candidates visible before the ticket
+    warp_topk4(hk, hi, a.k, a.cand_k + o, a.cand_i + o);
   }
-  __syncthreads();
-  if (tid == 0) {
-    *s_flag = (atomicAdd(a.slice_ticket + crank, 1) == T - 1);
-    __threadfence();
+  __syncthreads();  // every warp's candidates are written before the ticket is taken
+  if (tid == 0) {   // release this CTA's candidates; the last CTA acquires everyone's
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.slice_ticket + crank) : "memory");
+    *s_flag = old == T - 1;
   }
   for (int i = tid; i < kSlice * kUM; i += kUThreads) {
     const int rr = i / kUM, j = i % kUM;
@@ -395,42 +399,61 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
     if (rw < a.n && jg < m) a.logits[(size_t)rw * a.ld + jg] = F[i];
   }
   __syncthreads();
-  if (*s_flag) {  // last tile of this row slice: merge every tile's candidates
+  if (*s_flag) {  // last tile of this row slice: merge every tile's sorted candidates
     if (tid == 0) a.slice_ticket[crank] = 0;
     if (r < a.n) {
-      // each lane takes the (sorted) lists of tiles lane, lane + 32, ...
-      TopList<KMAX> M;
-      M.clear();
-      for (int t = lane; t < T; t += 32) {
-        const size_t o = ((size_t)t * kUN + r) * a.k;
-        float cv[KMAX];
-        int ci[KMAX];
-#pragma unroll
-        for (int q = 0; q < KMAX; ++q) {  // all loads first, then the inserts
-          cv[q] = q < a.k ? __ldcg(a.cand_v + o + q) : -__int_as_float(0x7f800000);
-          ci[q] = q < a.k ? __ldcg(a.cand_i + o + q) : kEmptyId;
-        }
-        if (t == lane) {  // the first list is already sorted
-#pragma unroll
-          for (int q = 0; q < KMAX; ++q) {
-            M.v[q] = cv[q];
-            M.id[q] = ci[q];
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < KMAX; ++q) M.insert(cv[q], ci[q]);
-        }
+      const int K = a.k;
+      uint32_t *ep = reinterpret_cast<uint32_t *>(gbase + kPartBytes + kSlice * kUM * 4);
+      uint32_t *Lk = ep + warp * 2 * kMergeWarpWords, *Li = Lk + kMergeWarpWords;
+      uint32_t *Rk = ep + kSlice * 2 * kMergeWarpWords + warp * 2 * NS_MAX_TOPK, *Ri = Rk + NS_MAX_TOPK;
+      for (int q = lane; q < K; q += kWarp) {
+        Rk[q] = 0u;
+        Ri[q] = (uint32_t)kEmptyId;
       }
-      float *wv = reinterpret_cast<float *>(gbase + kPartBytes + kSlice * kUM * 4) + warp * NS_MAX_TOPK;
-      int *wi = reinterpret_cast<int *>(gbase + kPartBytes + kSlice * kUM * 4 + kSlice * NS_MAX_TOPK * 4) +
-                warp * NS_MAX_TOPK;
-      warp_select<KMAX>(M, a.k, wv, wi);
-      __syncwarp();
-      if (lane < a.k) {
-        const int id = wi[lane];
-        const bool ok = id != kEmptyId;
-        a.out_ids[r * a.k + lane] = ok ? id : -1;
-        a.out_vals[r * a.k + lane] = ok ? wv[lane] : -__int_as_float(0x7f800000);
+      // up to kMergeLists tiles at a time, together with the running result
+      for (int t0 = 0; t0 < T; t0 += kMergeLists) {
+        const int nl = T - t0 < kMergeLists ? T - t0 : kMergeLists;
+        // entry e = l * K + q (list l, rank q) goes to Lk/Li[e]; each lane
+        // takes e = lane, lane + 32, ..., loading a batch before storing it
+        const int ne = nl * K, dl = kWarp / K, dq = kWarp - dl * K;
+        int l = lane / K, q = lane - (lane / K) * K;
+        for (int e0 = 0; e0 < ne; e0 += kMergeBatch * kWarp) {
+          uint32_t bk[kMergeBatch], bi[kMergeBatch];
+#pragma unroll
+          for (int b = 0; b < kMergeBatch; ++b) {
+            if (e0 + b * kWarp + lane < ne) {
+              const size_t src = ((size_t)(t0 + l) * kUN + r) * K + q;
+              bk[b] = __ldcg(a.cand_k + src);
+              bi[b] = __ldcg(a.cand_i + src);
+            }
+            q += dq;
+            l += dl;
+            if (q >= K) {
+              q -= K;
+              ++l;
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < kMergeBatch; ++b) {
+            const int e = e0 + b * kWarp + lane;
+            if (e < ne) {
+              Lk[e] = bk[b];
+              Li[e] = bi[b];
+            }
+          }
+        }
+        for (int q = lane; q < K; q += kWarp) {
+          Lk[nl * K + q] = Rk[q];
+          Li[nl * K + q] = Ri[q];
+        }
+        __syncwarp();
+        uint32_t lk, li;
+        warp_merge_lists(Lk, Li, nl + 1, K, Rk, Ri, lk, li);
+      }
+      if (lane < K) {
+        const uint32_t k = Rk[lane];
+        a.out_ids[r * K + lane] = k != 0u ? (int)Ri[lane] : -1;
+        a.out_vals[r * K + lane] = k != 0u ? key_value(k) : -__int_as_float(0x7f800000);
       }
     }
   }
@@ -474,9 +497,7 @@ int umma_tiles(int W_max) { return (W_max + kUM - 1) / kUM; }
 int umma_cluster() { return kUCluster; }
 
 cudaError_t prepare_umma_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(umma_step_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(umma_step_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
+  cudaError_t e = cudaFuncSetAttribute(umma_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
   if (e == cudaSuccess && !encoder()) e = cudaErrorNotSupported;
   return e;
 }
@@ -495,7 +516,7 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   a.k = L.k;
   a.logits = L.logits;
   a.ld = L.ld;
-  a.cand_v = L.cand_v;
+  a.cand_k = L.cand_k;
   a.cand_i = L.cand_i;
   a.slice_ticket = L.slice_ticket;
   a.out_ids = L.out_ids;
@@ -511,8 +532,7 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = L.programmatic ? 1 : 0;
-  if (L.k <= 16) return cudaLaunchKernelEx(&cfg, umma_step_kernel<16>, tmH, tmP, a);
-  return cudaLaunchKernelEx(&cfg, umma_step_kernel<32>, tmH, tmP, a);
+  return cudaLaunchKernelEx(&cfg, umma_step_kernel, tmH, tmP, a);
 }
 
 }  // namespace ns
