@@ -65,7 +65,7 @@ void layout(ns_handle *h, Carver &cv) {
     s.bitmap = cv.take<uint32_t>(d.nwords_pad);
     s.active = cv.take<int32_t>(c.W_max);
     s.count = cv.take<int32_t>(1);
-    s.length = cv.take<long long>(1);
+    s.length = cv.take<long long>(2);
     s.packed = cv.take<uint16_t>((size_t)c.W_max * c.H);
     s.logits = cv.take<float>((size_t)ns::kProjBN * d.ld_scratch);
     s.ppart = cv.take<float>((size_t)h->pgrid * ns::kProjBN * ns::kProjBM);

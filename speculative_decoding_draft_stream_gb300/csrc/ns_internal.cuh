@@ -30,7 +30,7 @@ struct SeqDev {
   uint32_t *bitmap;   // [nwords_pad] bit i%32 of word i/32 <=> id i in window
   int32_t *active;    // [W_max] I_t ascending
   int32_t *count;     // [1] |I_t|
-  long long *length;  // [1] |S|
+  long long *length;  // [2] |S|, then |S| mod W_max (the ring slot of the next entry)
   uint16_t *packed;   // [W_max x H] bf16 rows W_head[I_t[j], :]
   float *logits;      // [kProjBN x ld_scratch] fp32 logits when the caller passes none
   float *ppart;       // [proj_grid x kProjBN x kProjBM] split-K partial tiles

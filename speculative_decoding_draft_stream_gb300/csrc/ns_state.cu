@@ -199,7 +199,8 @@ __global__ void init_reset_kernel(SeqDev s, Dims d) {
     if (i < d.nwords_pad) s.bitmap[i] = 0u;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    *s.length = 0;
+    s.length[0] = 0;
+    s.length[1] = 0;
     *s.count = 0;
   }
 }
@@ -273,7 +274,10 @@ __global__ void __launch_bounds__(kStateThreads) init_compose_kernel(SeqDev s, D
     atomicAdd(&s.counts[x], 1u);
     atomicOr(&s.bitmap[x >> 5], 1u << (x & 31));
   }
-  if (threadIdx.x == 0) *s.length = Ltot;
+  if (threadIdx.x == 0) {
+    s.length[0] = Ltot;
+    s.length[1] = Ltot % d.W_max;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -339,6 +343,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
   __shared__ uint32_t h_old[kHashSlots];
   __shared__ int s_misc[4];
   __shared__ long long s_len;
+  __shared__ int s_head;  // |S| mod W_max
   __shared__ __align__(8) unsigned long long s_bar;  // the bitmap copy
   __shared__ int sh_scan[2 * kWarp];
 
@@ -405,7 +410,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
 
   // ---- leader prologue: |S|, the tree ids -----------------------------------
   if (leader) {
-    if (tid == 0) s_len = *s.length;
+    if (tid == 0) {  // |S| and the ring slot of the next entry, one 16-byte load
+      const longlong2 lv = *reinterpret_cast<const longlong2 *>(s.length);
+      s_len = lv.x;
+      s_head = (int)lv.y;
+    }
     if (tid < n_tree) s_tree[tid] = tree[tid];
     for (int q = tid; q < kHashSlots; q += blockDim.x) {
       h_key[q] = -1;
@@ -418,12 +427,15 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
   }
   __syncthreads();  // the leader's s_len and s_tree; its barrier is initialised
 
-  const long long W = d.W_max;
+  const int W = d.W_max;
   const long long len0 = s_len;
   const long long old_start = len0 > W ? len0 - W : 0;
-  const int max_ev = (int)((n_tree + K) < W ? (n_tree + K) : W);  // no step evicts more
+  const int max_ev = (n_tree + K) < W ? (n_tree + K) : W;  // no step evicts more
   int ev_id = -1;
-  if (leader && tid < max_ev) ev_id = s.ring[(old_start + tid) % W];  // used after the ranking
+  if (leader && tid < max_ev) {  // position old_start + tid (old_start = len0 - W past a full window)
+    const int r0 = len0 > W ? s_head : 0;
+    ev_id = s.ring[r0 + tid >= W ? r0 + tid - W : r0 + tid];  // used after the ranking
+  }
 
   // ---- rank the slice -------------------------------------------------------
   for (int c0 = 0; c0 < nslice; c0 += kRankPass) {
@@ -537,6 +549,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
     if (keep_a) s_app[__popc(ba & lt)] = a;
     if (keep_b) s_app[__popc(ba) + __popc(bb & lt)] = b;
     if (lane == 0) s_misc[2] = __popc(ba) + __popc(bb);
+    asm volatile("bar.arrive 1, 64;" ::: "memory");  // C_draft and its length, for warp 0
   }
   uint32_t ev_cnt = 0u;
   if (ev_id >= 0) {
@@ -562,35 +575,41 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
     return;
   }
 
-  if (K > 0 && warp == 0) {
-    uint32_t lk, li;
-    warp_merge_lists(cl_k, cl_i, nct, K, res_k, res_i, lk, li);
+  // Warp 0 merges the CTAs' Top-K and appends C_ver after C_draft: the
+  // ranked ids are best first; a row without enough orderable (non-NaN)
+  // values leaves empty slots at the end, which are not appended.
+  if (warp == 0) {
+    asm volatile("bar.sync 1, 64;" ::: "memory");  // warp 1 has written C_draft
+    const int n_draft = s_misc[2];
+    int n_ver = 0;
+    if (K > 0) {
+      uint32_t lk, li;
+      warp_merge_lists(cl_k, cl_i, nct, K, res_k, res_i, lk, li);
+      const bool ok = lane < K && res_k[lane] != 0u;
+      n_ver = __popc(__ballot_sync(0xffffffffu, ok));
+      if (ok) {
+        int y = (int)res_i[lane];
+        if ((unsigned)y >= (unsigned)d.V) {  // cannot happen for a well-formed merge
+          set_flag(err, NS_FLAG_INTERNAL | (1u << 8));
+          y = 0;
+        }
+        s_app[n_draft + lane] = y;
+      }
+    }
+    if (lane == 0) {
+      if (n_ver < K) set_flag(err, NS_FLAG_BAD_ID);
+      s_misc[3] = n_draft + n_ver;
+    }
   }
   if (tid < max_ev) {
     s_evict[tid] = ev_id;
     s_evc[tid] = ev_cnt;
   }
-  __syncthreads();
+  __syncthreads();  // the appended entries, their count and the evictable ids
   // Let a programmatically launched successor start its prologue; it waits
   // for this grid's results before reading them.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-  const int n_draft = s_misc[2];
-  // C_ver: the ranked ids are best first; a row without enough orderable
-  // (non-NaN) values leaves empty slots at the end, which are not appended.
-  int n_ver = 0;
-  for (int q = 0; q < K; ++q) n_ver += res_k[q] != 0u;
-  if (tid < n_ver) {
-    int y = (int)res_i[tid];
-    if ((unsigned)y >= (unsigned)d.V) {  // cannot happen for a well-formed merge
-      set_flag(err, NS_FLAG_INTERNAL | (1u << 8));
-      y = 0;
-    }
-    s_app[n_draft + tid] = y;
-  }
-  if (tid == 0 && n_ver < K) set_flag(err, NS_FLAG_BAD_ID);
-  const int m = n_draft + n_ver;
-  __syncthreads();  // C_ver is in s_app before anyone reads the appended entries
+  const int m = s_misc[3];
 
   // ---- window: what enters (+1), what leaves (-1), net per distinct id -----
   const long long len1 = len0 + m;
@@ -622,11 +641,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
       }
     }
   }
-  if (tid < n_ap) {
-    const long long p = ap_begin + tid;
-    s.ring[p % W] = s_app[p - len0];
+  if (tid < n_ap) {  // position p = ap_begin + tid goes to ring[p % W]
+    const int off = (int)(ap_begin - len0) + tid;
+    s.ring[(s_head + off) % W] = s_app[off];
   }
-  if (tid == 0) *s.length = len1;
+  if (tid == 0) {
+    s.length[0] = len1;
+    s.length[1] = (s_head + m) % W;
+  }
   // The bitmap copy must have landed before its bits are read.  If the wait
   // gave up (NS_FLAG_TIMEOUT), the bitmap and I_t are left as they were.
   const bool have_bits = __syncthreads_and(mbar_wait(smem_u32(&s_bar), 0, err));

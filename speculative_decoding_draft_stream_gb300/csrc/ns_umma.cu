@@ -5,9 +5,10 @@
 // Eq. 1 restricted to the active rows).
 //
 // Tile: 128 W_head rows (UMMA M) x 64 hidden rows (UMMA N, n <= 64).
-// Each tile belongs to one cluster of 8 CTAs that split H eight ways; the
-// 64-wide k slices are dealt round-robin (CTA c takes slices c, c+8, ...),
-// so at any moment a cluster reads 1 KB runs of each row.
+// Each tile belongs to one cluster of C CTAs (16 where the device holds such
+// clusters, else 8) that split H C ways; the 64-wide k slices are dealt
+// round-robin (CTA c takes slices c, c+C, ...), so at any moment a cluster
+// reads C * 128-byte runs of each row.
 // Per CTA and per k slice (a 4-stage ring overlaps the roles):
 //   * warps 4-7 gather the tile's 128 rows with 16-byte cp.async (four rows
 //     of 128 contiguous bytes per warp instruction) into the 128-byte-
@@ -22,8 +23,8 @@
 //     TMA tile store, so each W_head row crosses HBM once per step.
 // Epilogue: warps 4-7 read the accumulator (tcgen05.ld, one row per thread),
 // every CTA publishes its partial tile in shared memory, and after a cluster
-// barrier CTA c adds the eight partials for hidden rows [8c, 8c+8) through
-// distributed shared memory in a fixed order (deterministic), ranks each
+// barrier CTA c adds the C partials for hidden rows [64c/C, 64(c+1)/C)
+// through distributed shared memory in a fixed order (deterministic), ranks each
 // row's 128 columns (one warp per row) and writes those logits.  The
 // per-tile candidates (sorted) of a row slice are merged by the last CTA of
 // that slice to finish (release/acquire ticket) into the final top-k.
@@ -46,7 +47,6 @@ constexpr int kUM = 128;                     // W rows per tile
 constexpr int kUN = 64;                      // hidden rows per tile
 constexpr int kUK = 64;                      // k per stage: one 128-byte swizzled row
 constexpr int kUStages = 4;
-constexpr int kUCluster = 8;                 // K splits per tile = CTAs per cluster
 constexpr int kUThreads = 256;
 constexpr int kGatherThreads = 128;          // warps 4-7
 constexpr int kInFlight = 3;                 // cp.async stages a gather thread keeps in flight
@@ -56,7 +56,6 @@ constexpr int kStoresInFlight = 1;           // packed-buffer stores still readi
 // the release of the stage they reuse kUStages iterations on.  Reuse can only
 // make progress when the two lags fit in the ring.
 static_assert((kInFlight - 1) + kStoresInFlight <= kUStages - 1, "stage ring too short for the pipeline lags");
-constexpr int kSlice = kUN / kUCluster;      // hidden rows reduced by one CTA
 constexpr int kStageA = kUM * kUK * 2;       // 16 KB
 constexpr int kStageB = kUN * kUK * 2;       // 8 KB
 constexpr int kStage = kStageA + kStageB;    // 24 KB (1024-byte multiple)
@@ -69,7 +68,8 @@ constexpr uint32_t kTmemCols = 64;
 constexpr int kMergeLists = 24;  // tiles' lists merged per round of the final merge (+ the running list)
 constexpr int kMergeWarpWords = (kMergeLists + 1) * NS_MAX_TOPK;
 constexpr int kMergeBatch = 8;   // candidate loads a lane keeps in flight while staging
-static_assert(kPartBytes + kSlice * kUM * 4 + kSlice * (2 * kMergeWarpWords + 2 * NS_MAX_TOPK) * 4 <= kRingBytes,
+// hidden rows reduced by one CTA: kUN / cluster size, at most 8
+static_assert(kPartBytes + 8 * kUM * 4 + 8 * (2 * kMergeWarpWords + 2 * NS_MAX_TOPK) * 4 <= kRingBytes,
               "epilogue buffers reuse the stage ring");
 
 // D = fp32, A = B = bf16, both K-major, N = 64, M = 128.
@@ -179,15 +179,17 @@ struct UmmaArgs {
   int32_t ld;
   uint32_t *cand_k;          // [tiles x 64 x k] per-tile candidates: order keys, best first
   uint32_t *cand_i;          // and their ids
-  int32_t *slice_ticket;     // [kUCluster]
+  int32_t *slice_ticket;     // [cluster size]
   int32_t *out_ids;          // [n x k]
   float *out_vals;
   uint32_t *err;
 };
 
+template <int kUCluster>
 __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1)
     umma_step_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmP,
                      UmmaArgs a) {
+  constexpr int kSlice = kUN / kUCluster;  // hidden rows [kSlice * c, kSlice * (c + 1)) are reduced by CTA c
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte-swizzled tiles need 1024-byte alignment
@@ -355,8 +357,8 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
 
   // ---- reduce hidden rows [8c, 8c+8) over the eight partials ---------------
   float *F = reinterpret_cast<float *>(gbase + kPartBytes);  // [8][128]
-  {
-    const int rr = tid / (kUM / 4), j = (tid % (kUM / 4)) * 4;  // 256 threads cover 8 x 128
+  if (tid < kSlice * (kUM / 4)) {
+    const int rr = tid / (kUM / 4), j = (tid % (kUM / 4)) * 4;  // a float4 of the kSlice x 128 block each
     const uint32_t off = base + (uint32_t)(((crank * kSlice + rr) * kUM + j) * 4);
     float4 s4 = ld_peer_f4(map_peer(off, 0));
 #pragma unroll
@@ -376,7 +378,8 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
   // is ascending, so ids ascend with the column), and k rounds of a warp-wide
   // best-of-heads write the tile's k best, best first, with global ids.
   const int r = (int)crank * kSlice + warp;
-  if (r < a.n) {
+  const bool row_warp = warp < kSlice && r < a.n;
+  if (row_warp) {
     uint32_t hk[4], hi[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -401,7 +404,7 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
   __syncthreads();
   if (*s_flag) {  // last tile of this row slice: merge every tile's sorted candidates
     if (tid == 0) a.slice_ticket[crank] = 0;
-    if (r < a.n) {
+    if (row_warp) {
       const int K = a.k;
       uint32_t *ep = reinterpret_cast<uint32_t *>(gbase + kPartBytes + kSlice * kUM * 4);
       uint32_t *Lk = ep + warp * 2 * kMergeWarpWords, *Li = Lk + kMergeWarpWords;
@@ -494,12 +497,44 @@ bool encode_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t ou
 }  // namespace
 
 int umma_tiles(int W_max) { return (W_max + kUM - 1) / kUM; }
-int umma_cluster() { return kUCluster; }
+// Clusters of 16 CTAs halve each CTA's share of H (a shorter gather chain)
+// but fewer of them fit at once; a launch uses them only when every tile of
+// W_max gets a cluster in one wave.
+int g_max16 = 0;  // resident 16-CTA clusters, from prepare_umma_kernels
+
+int umma_cluster() { return 16; }  // the most row slices a launch can use
+
+// How many clusters of 16 fused-kernel CTAs can be resident at once.
+int max_clusters16() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(16, 1, 1);
+  cfg.blockDim = dim3(kUThreads, 1, 1);
+  cfg.dynamicSmemBytes = kUSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 16;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, umma_step_kernel<16>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return clusters;
+}
 
 cudaError_t prepare_umma_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(umma_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
-  if (e == cudaSuccess && !encoder()) e = cudaErrorNotSupported;
-  return e;
+  cudaError_t e = cudaFuncSetAttribute(umma_step_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(umma_step_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(umma_step_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  if (!encoder()) return cudaErrorNotSupported;
+  g_max16 = max_clusters16();
+  return cudaSuccess;
 }
 
 cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
@@ -523,7 +558,8 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   a.out_vals = L.out_vals;
   a.err = L.err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(umma_tiles(L.W_max) * kUCluster));
+  const int CL = umma_tiles(L.W_max) <= g_max16 ? 16 : 8;
+  cfg.gridDim = dim3((unsigned)(umma_tiles(L.W_max) * CL));
   cfg.blockDim = dim3(kUThreads);
   cfg.dynamicSmemBytes = kUSmem;
   cfg.stream = st;
@@ -532,7 +568,8 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = L.programmatic ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, umma_step_kernel, tmH, tmP, a);
+  if (CL == 16) return cudaLaunchKernelEx(&cfg, umma_step_kernel<16>, tmH, tmP, a);
+  return cudaLaunchKernelEx(&cfg, umma_step_kernel<8>, tmH, tmP, a);
 }
 
 }  // namespace ns
