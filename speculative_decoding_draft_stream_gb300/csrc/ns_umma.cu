@@ -186,7 +186,7 @@ struct UmmaArgs {
 };
 
 template <int kUCluster>
-__global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1)
+__global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2)
     umma_step_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmP,
                      UmmaArgs a) {
   constexpr int kSlice = kUN / kUCluster;  // hidden rows [kSlice * c, kSlice * (c + 1)) are reduced by CTA c
@@ -203,7 +203,8 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = cluster_rank();
-  const int tile = blockIdx.x / kUCluster;
+  // clusters take tiles tile0, tile0 + ncl, ... (one each when the grid holds them all)
+  const int tile0 = blockIdx.x / kUCluster, ncl = gridDim.x / kUCluster;
 
   // ---- prologue (overlaps the state update when launched programmatically) --
   if (tid == 0) {
@@ -225,8 +226,8 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
   grid_dependency_wait();  // I_t and |I_t| come from the state update
   const int m = *a.count_ptr;
   const int T = (m + kUM - 1) / kUM;
-  if (tile >= T) {  // uniform across the cluster
-    if (T == 0 && tile == 0) {
+  if (tile0 >= T) {  // uniform across the cluster
+    if (T == 0 && tile0 == 0) {
       const int r = (int)crank * kSlice + warp;
       if (warp < kSlice && r < a.n && lane < a.k) {
         a.out_ids[r * a.k + lane] = -1;
@@ -239,8 +240,11 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
   }
 
   const int KC = a.H / kUK;
-  // k slices of this CTA: crank, crank + 8, ... (nk of them)
+  // k slices of this CTA: crank, crank + C, ... (nk of them, the same for every tile)
   const int nk = KC > (int)crank ? (KC - (int)crank + kUCluster - 1) / kUCluster : 0;
+  // Stage use g = iter * nk + kt runs on across tiles: ring slot g % kUStages,
+  // mbarrier phase g / kUStages.
+  for (int tile = tile0, iter = 0; tile < T; tile += ncl, ++iter) {
   const int row0 = tile * kUM;
   if (tid < kUM) {
     const int j = row0 + tid;
@@ -257,26 +261,29 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
   if (warp == 0 && lane == 0) {  // hidden slices by TMA
     int issued = 0;
     for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % kUStages;
-      if (kt >= kUStages && !mbar_wait(bar_empty + 8 * s, ((kt / kUStages) - 1) & 1, a.err)) break;
+      const int g = iter * nk + kt, s = g % kUStages;
+      if (g >= kUStages && !mbar_wait(bar_empty + 8 * s, ((g / kUStages) - 1) & 1, a.err)) break;
       issued = kt + 1;
       mbar_expect_tx(bar_full + 8 * s, kStageB);
       tma_load_2d(base + s * kStage + kStageA, &tmH, ((int)crank + kt * kUCluster) * kUK, 0, bar_full + 8 * s);
     }
     // nothing may still be landing in shared memory when the CTA leaves
     const int first = issued > kUStages ? issued - kUStages : 0;
-    for (int kt = first; kt < issued; ++kt) mbar_wait(bar_full + 8 * (kt % kUStages), (kt / kUStages) & 1, a.err);
+    for (int kt = first; kt < issued; ++kt) {
+      const int g = iter * nk + kt;
+      mbar_wait(bar_full + 8 * (g % kUStages), (g / kUStages) & 1, a.err);
+    }
   } else if (warp >= 4) {  // W_head rows by cp.async
     const int p = tid - 128, wl = p >> 5, c = lane & 7;
     int arrived = 0;
     for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % kUStages;
-      if (kt >= kUStages) mbar_wait(bar_empty + 8 * s, ((kt / kUStages) - 1) & 1, a.err);
+      const int g = iter * nk + kt, s = g % kUStages;
+      if (g >= kUStages) mbar_wait(bar_empty + 8 * s, ((g / kUStages) - 1) & 1, a.err);
       const uint32_t A = base + s * kStage;
       const int col = ((int)crank + kt * kUCluster) * kUK + c * 8;
 #pragma unroll
-      for (int it = 0; it < kUM / 16; ++it) {
-        const int row = it * 16 + wl * 4 + (lane >> 3);
+      for (int rg = 0; rg < kUM / 16; ++rg) {
+        const int row = rg * 16 + wl * 4 + (lane >> 3);
         const uint16_t *src = a.W + (size_t)s_rows[row] * a.H + col;
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(A + row * 128 + ((c ^ (row & 7)) << 4)),
                      "l"(src)
@@ -286,18 +293,18 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
       if (kt + 1 - arrived >= kInFlight) {  // the oldest pending stage has landed: publish it
         asm volatile("cp.async.wait_group %0;" ::"n"(kInFlight - 1) : "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(bar_full + 8 * (arrived % kUStages));
+        mbar_arrive(bar_full + 8 * ((iter * nk + arrived) % kUStages));
         ++arrived;
       }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    for (; arrived < nk; ++arrived) mbar_arrive(bar_full + 8 * (arrived % kUStages));
+    for (; arrived < nk; ++arrived) mbar_arrive(bar_full + 8 * ((iter * nk + arrived) % kUStages));
   } else if (warp == 1 && lane == 0) {
     bool ok = true;
     for (int kt = 0; kt < nk && ok; ++kt) {
-      const int s = kt % kUStages;
-      ok = mbar_wait(bar_full + 8 * s, (kt / kUStages) & 1, a.err);
+      const int g = iter * nk + kt, s = g % kUStages;
+      ok = mbar_wait(bar_full + 8 * s, (g / kUStages) & 1, a.err);
       if (!ok) break;
       tc_fence_after();
       const uint32_t A = base + s * kStage;
@@ -311,47 +318,46 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
   } else if (warp == 2 && lane == 0) {
     int released = 0;
     for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % kUStages;
-      if (!mbar_wait(bar_full + 8 * s, (kt / kUStages) & 1, a.err)) break;
+      const int g = iter * nk + kt, s = g % kUStages;
+      if (!mbar_wait(bar_full + 8 * s, (g / kUStages) & 1, a.err)) break;
       tma_store_2d(&tmP, base + s * kStage, ((int)crank + kt * kUCluster) * kUK, row0);
       bulk_commit();
       if (kt + 1 - released > kStoresInFlight) {  // the oldest store has read its stage
         asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kStoresInFlight) : "memory");
-        mbar_arrive(bar_empty + 8 * (released % kUStages));
+        mbar_arrive(bar_empty + 8 * ((iter * nk + released) % kUStages));
         ++released;
       }
     }
     bulk_wait_read_all();
-    for (; released < nk; ++released) mbar_arrive(bar_empty + 8 * (released % kUStages));
+    for (; released < nk; ++released) mbar_arrive(bar_empty + 8 * ((iter * nk + released) % kUStages));
     bulk_wait_all();
   }
 
   // ---- epilogue: accumulator -> partial tile in shared memory ---------------
-  float v[kUN];
+  tc_fence_before();
+  __syncthreads();  // every role is done with the ring (MMAs issued, packed stores have read it)
+  float *P = reinterpret_cast<float *>(gbase);  // [64][128] partial of this CTA
   if (warp >= 4) {
     // tcgen05.ld is warp-collective: the whole warp takes the same branch
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_acc, 0, a.err));
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_acc, iter & 1, a.err));
     tc_fence_after();
-    if (nk > 0 && ok) {
-      const uint32_t t0 = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    const int j = (warp - 4) * 32 + lane;
+    const uint32_t t0 = tmem + ((uint32_t)((warp - 4) * 32) << 16);
 #pragma unroll
-      for (int c = 0; c < kUN; c += 16) tmem_ld16(t0 + c, v + c);
-      tmem_ld_wait();
-    } else {
+    for (int c = 0; c < kUN; c += 16) {
+      float v[16];
+      if (nk > 0 && ok) {
+        tmem_ld16(t0 + c, v);
+        tmem_ld_wait();
+      } else {
 #pragma unroll
-      for (int c = 0; c < kUN; ++c) v[c] = 0.f;
+        for (int q = 0; q < 16; ++q) v[q] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) P[(c + q) * kUM + j] = v[q];
     }
   }
   tc_fence_before();
-  __syncthreads();  // MMAs, TMEM reads and packed stores are all done with the ring
-  __syncwarp();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-  float *P = reinterpret_cast<float *>(gbase);  // [64][128] partial of this CTA
-  if (warp >= 4) {
-    const int j = (warp - 4) * 32 + lane;
-#pragma unroll
-    for (int r = 0; r < kUN; ++r) P[r * kUM + j] = v[r];
-  }
   __syncwarp();
   cluster_sync();
 
@@ -462,6 +468,9 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
   }
   __syncwarp();
   cluster_sync();  // peers may still be reading this CTA's partial tile
+  }  // tiles
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---- host side ---------------------------------------------------------------
@@ -497,28 +506,30 @@ bool encode_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t ou
 }  // namespace
 
 int umma_tiles(int W_max) { return (W_max + kUM - 1) / kUM; }
-// Clusters of 16 CTAs halve each CTA's share of H (a shorter gather chain)
-// but fewer of them fit at once; a launch uses them only when every tile of
-// W_max gets a cluster in one wave.
-int g_max16 = 0;  // resident 16-CTA clusters, from prepare_umma_kernels
+// Clusters of 16 CTAs halve each CTA's share of H (a shorter gather chain),
+// so they are used wherever the device holds them.  The grid has one
+// cluster per tile of W_max, capped at the clusters that are resident at
+// once; a cluster loops over tiles when |I_t| needs more.
+int g_max16 = 0, g_max8 = 0;  // resident clusters of each size, from prepare_umma_kernels
 
 int umma_cluster() { return 16; }  // the most row slices a launch can use
 
-// How many clusters of 16 fused-kernel CTAs can be resident at once.
-int max_clusters16() {
+// How many clusters of `CL` fused-kernel CTAs can be resident at once.
+template <int CL>
+int max_clusters() {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(16, 1, 1);
+  cfg.gridDim = dim3(CL, 1, 1);
   cfg.blockDim = dim3(kUThreads, 1, 1);
   cfg.dynamicSmemBytes = kUSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 16;
+  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, umma_step_kernel<16>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, umma_step_kernel<CL>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -533,8 +544,9 @@ cudaError_t prepare_umma_kernels() {
     e = cudaFuncSetAttribute(umma_step_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   if (!encoder()) return cudaErrorNotSupported;
-  g_max16 = max_clusters16();
-  return cudaSuccess;
+  g_max16 = max_clusters<16>();
+  g_max8 = max_clusters<8>();
+  return g_max16 > 0 || g_max8 > 0 ? cudaSuccess : cudaErrorNotSupported;
 }
 
 cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
@@ -558,8 +570,10 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   a.out_vals = L.out_vals;
   a.err = L.err;
   cudaLaunchConfig_t cfg = {};
-  const int CL = umma_tiles(L.W_max) <= g_max16 ? 16 : 8;
-  cfg.gridDim = dim3((unsigned)(umma_tiles(L.W_max) * CL));
+  const int CL = g_max16 > 0 ? 16 : 8;
+  const int resident = CL == 16 ? g_max16 : g_max8;
+  const int ncl = umma_tiles(L.W_max) < resident ? umma_tiles(L.W_max) : resident;
+  cfg.gridDim = dim3((unsigned)(ncl * CL));
   cfg.blockDim = dim3(kUThreads);
   cfg.dynamicSmemBytes = kUSmem;
   cfg.stream = st;
