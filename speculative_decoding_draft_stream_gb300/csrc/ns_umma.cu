@@ -174,7 +174,7 @@ struct UmmaArgs {
   const uint16_t *W;         // W_head [V x H]
   const int32_t *idx;        // I_t ascending
   const int32_t *count_ptr;  // |I_t|
-  int32_t V, H, n, k;
+  int32_t V, H, n, k, W_max;
   float *logits;             // [n x ld]
   int32_t ld;
   uint32_t *cand_k;          // [tiles x 64 x k] per-tile candidates: order keys, best first
@@ -224,6 +224,10 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
   const uint32_t tmem = *tmem_slot;
 
   grid_dependency_wait();  // I_t and |I_t| come from the state update
+  // The first tile's row ids load together with |I_t| (one round trip); the
+  // entries past |I_t| are not used.
+  int id_first = 0;
+  if (tid < kUM && tile0 * kUM + tid < a.W_max) id_first = a.idx[tile0 * kUM + tid];
   const int m = *a.count_ptr;
   const int T = (m + kUM - 1) / kUM;
   if (tile0 >= T) {  // uniform across the cluster
@@ -248,13 +252,17 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
   const int row0 = tile * kUM;
   if (tid < kUM) {
     const int j = row0 + tid;
-    int id = a.idx[j < m ? j : m - 1];  // rows past |I_t| repeat the last active row
-    if ((unsigned)id >= (unsigned)a.V) {  // I_t only holds valid ids
-      atomicOr(a.err, NS_FLAG_INTERNAL | (3u << 8));
-      id = 0;
+    if (j < m) {
+      int id = iter == 0 ? id_first : a.idx[j];
+      if ((unsigned)id >= (unsigned)a.V) {  // I_t only holds valid ids
+        atomicOr(a.err, NS_FLAG_INTERNAL | (3u << 8));
+        id = 0;
+      }
+      s_rows[tid] = id;
     }
-    s_rows[tid] = id;
   }
+  __syncthreads();
+  if (tid < kUM && row0 + tid >= m) s_rows[tid] = s_rows[m - 1 - row0];  // rows past |I_t| repeat the last
   __syncthreads();
 
   // ---- main loop -------------------------------------------------------------
@@ -558,6 +566,7 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   a.idx = L.idx;
   a.count_ptr = L.count_ptr;
   a.V = L.V;
+  a.W_max = L.W_max;
   a.H = L.H;
   a.n = L.n;
   a.k = L.k;
