@@ -35,7 +35,9 @@ Readings where the pages are silent (each also listed in the design notes):
 2. Append everything the formal definition appends, so a re-seen id refreshes
    its recency (duplicates between C_draft and C_ver are kept too).
 3. Ties in T_K: larger value first, then the smaller id.  Comparisons are made
-   on the fp32 inputs exactly (fp64 holds every fp32 value).
+   on the fp32 inputs exactly (fp64 holds every fp32 value); -0.0 ties +0.0.
+   NaN never ranks; -inf and +inf are ordered like any other value.  A row
+   with fewer than K orderable (non-NaN) values gives fewer than K picks.
 4. Unique() yields ascending ids.
 5. Suffix of a stream shorter than W_max is the whole stream.
 6. Prompt ids are kept verbatim (with repeats); only the Top-K union is
@@ -46,7 +48,6 @@ Readings where the pages are silent (each also listed in the design notes):
 9. Top-k of a row with fewer than k active columns is padded with id -1 and
    value -inf.
 
-Preconditions: logits are finite (ordering of NaN is undefined).
 """
 
 from __future__ import annotations
@@ -76,34 +77,44 @@ def top_k_rows(Z, K: int) -> np.ndarray:
     """T_K of every row of Z, as ordered index lists (int64 [rows, min(K, V)]).
 
     Pick r (r = 0..K-1) is the largest value not yet picked; among equal
-    values the smallest index wins (numpy's argmax returns the first maximum).
-    This is exactly the first K entries of a stable descending sort.  Picked
-    entries are set to -inf, which no finite input can reach, so no index is
-    picked twice.
+    values the smallest index wins.  This is exactly the first K entries of a
+    stable descending sort of the row's orderable (non-NaN) values.  Rows of
+    finite values take K rounds of argmax (numpy's argmax returns the first
+    maximum; picked entries are set to -inf, which no finite input reaches);
+    rows holding NaN or an infinity are sorted.  A row with fewer than K
+    orderable values is padded with -1.
     """
     Z = np.asarray(Z, dtype=np.float32)
     if Z.ndim != 2:
         raise ValueError("top_k_rows expects a 2-D array")
     n, V = Z.shape
     K = min(int(K), V)
-    out = np.empty((n, max(K, 0)), dtype=np.int64)
+    out = np.full((n, max(K, 0)), -1, dtype=np.int64)
     if K <= 0 or n == 0:
         return out
-    if not np.all(np.isfinite(Z)):
-        raise ValueError("logits must be finite")
-    rows = np.arange(n)
-    work = Z.astype(np.float64)
-    for r in range(K):
-        j = np.argmax(work, axis=1)
-        out[:, r] = j
-        work[rows, j] = -np.inf
+    finite = np.all(np.isfinite(Z), axis=1)
+    rows = np.flatnonzero(finite)
+    if len(rows):
+        work = Z[rows].astype(np.float64)
+        sel = np.arange(len(rows))
+        for r in range(K):
+            j = np.argmax(work, axis=1)
+            out[rows, r] = j
+            work[sel, j] = -np.inf
+    for i in np.flatnonzero(~finite):
+        z = Z[i].astype(np.float64)
+        ids = np.flatnonzero(~np.isnan(z))
+        order = ids[np.lexsort((ids, -z[ids]))]  # value descending, then id ascending
+        take = order[:K]
+        out[i, :len(take)] = take
     return out
 
 
 def top_k(z, K: int) -> List[int]:
-    """T_K(z) of one logit vector, best first."""
+    """T_K(z) of one logit vector, best first (fewer than K ids when the
+    vector has fewer than K orderable values)."""
     z = np.asarray(z, dtype=np.float32).reshape(1, -1)
-    return [int(x) for x in top_k_rows(z, K)[0]]
+    return [int(x) for x in top_k_rows(z, K)[0] if x >= 0]
 
 
 # ---------------------------------------------------------------------------
@@ -129,7 +140,7 @@ def stream_init(prompt: Sequence[int], prefill_logits, K_pre: int, row_chunk: in
         for i in range(T.shape[0]):
             for x in T[i]:
                 x = int(x)
-                if x not in seen:
+                if x >= 0 and x not in seen:  # -1 pads a row with fewer than K_pre orderable values
                     seen.add(x)
                     S.append(x)
     return S

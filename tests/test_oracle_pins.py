@@ -15,6 +15,7 @@ fails at least one test:
 
 import json
 import os
+import math
 import random
 
 import numpy as np
@@ -98,9 +99,22 @@ def test_topk_signed_zero_is_a_tie():
     assert O.top_k(z, 2) == [0, 1]
 
 
-def test_topk_rejects_nonfinite():
-    with pytest.raises(ValueError):
-        O.top_k(np.array([1.0, np.nan], np.float32), 1)
+def _brute_topk_nan(z, K):
+    """First K of a stable descending sort of the non-NaN entries."""
+    return sorted((i for i in range(len(z)) if not math.isnan(float(z[i]))), key=lambda i: (-float(z[i]), i))[:K]
+
+
+def test_topk_nan_never_ranks_and_infinities_order():
+    rng = random.Random(99)
+    for _ in range(300):
+        V = rng.randint(1, 30)
+        K = rng.randint(0, V + 2)
+        z = np.array([rng.choice([np.nan, -np.inf, np.inf, -0.0, 0.0, -1.0, 2.5]) for _ in range(V)], np.float32)
+        assert O.top_k(z, K) == _brute_topk_nan(z, K)
+    Z = np.array([[np.nan, 1.0, np.nan, -np.inf], [2.0, 2.0, 1.0, 0.0]], np.float32)
+    assert O.top_k_rows(Z, 3).tolist() == [[1, 3, -1], [0, 1, 2]]
+    # a prefill row with fewer than K_pre orderable values adds only those
+    assert O.stream_init([5], np.array([[np.nan, 3.0, np.nan, np.nan]], np.float32), 2) == [5, 1]
 
 
 # ---------------------------------------------------------------------------
