@@ -305,8 +305,8 @@ __device__ __forceinline__ uint32_t leader_addr(const void *p) {
   return r;
 }
 
-// The cluster's CTAs rank one slice each of the verify row and hand their Top-K
-// to the leader through distributed shared memory.  A CTA ranks its slice in
+// The cluster's CTAs other than the leader rank one slice each of the verify
+// row and hand their Top-K to the leader through distributed shared memory.  A CTA ranks its slice in
 // passes of 16 values per thread, held in registers: each thread takes the
 // best of its 16; the K-th best of those 1024 maxima is a threshold T that
 // every value of the pass's Top-K reaches, and only values at or above T (at
@@ -370,10 +370,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   // ---- this CTA's slice of the verify row; the first pass's loads ----------
+  // The leader ranks nothing when the cluster has other CTAs: its own loads
+  // (|S|, the tree, the ring slots and counts it will update) overlap their
+  // ranking instead of delaying its share of it.
   int lo = 0, nslice = 0;
-  if (K > 0) {
-    const int S = ((d.V / 4 + nct - 1) / nct) * 4;  // values per CTA, a multiple of 4
-    lo = (int)rank * S;
+  const int nrank = nct > 1 ? nct - 1 : 1, slice = nct > 1 ? (int)rank - 1 : 0;
+  if (K > 0 && slice >= 0) {
+    const int S = (((d.V + 3) / 4 + nrank - 1) / nrank) * 4;  // values per ranking CTA, a multiple of 4
+    lo = slice * S;
     nslice = d.V - lo < S ? d.V - lo : S;
     if (nslice < 0) nslice = 0;
   }
@@ -405,6 +409,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
   auto id_of = [&](int c0, int q) -> uint32_t {
     return VEC ? (uint32_t)(lo + c0 + 4 * ((q >> 2) * kStateThreads + tid) + (q & 3))
                : (uint32_t)(lo + c0 + q * kStateThreads + tid);
+  };
+  // whether group g (x[4g .. 4g+3]) holds any value of the pass starting at c0
+  // (the rest of the thread's slots are padding; uniform across most warps)
+  auto group_live = [&](int c0, int g) -> bool {
+    const int n = nslice - c0 < kRankPass ? nslice - c0 : kRankPass;
+    return VEC ? 4 * (g * kStateThreads + tid) < n : 4 * g * kStateThreads + tid < n;
   };
   if (nslice > 0) load_pass(0);
 
@@ -445,10 +455,15 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
     float mv = -__int_as_float(0x7f800000);
     int mq = -1;
 #pragma unroll
-    for (int q = 0; q < kRankPer; ++q) {
-      if (x[q] > mv) {
-        mv = x[q];
-        mq = q;
+    for (int g = 0; g < kRankPer / 4; ++g) {
+      if (group_live(c0, g)) {
+#pragma unroll
+        for (int q = 4 * g; q < 4 * g + 4; ++q) {
+          if (x[q] > mv) {
+            mv = x[q];
+            mq = q;
+          }
+        }
       }
     }
     if (mq < 0) {  // nothing above -inf: the first -inf, if any
@@ -494,16 +509,22 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
     const uint32_t tk = s_thr[0], ti = s_thr[1];
     const float tv = tk != 0u ? key_value(tk) : -__int_as_float(0x7f800000);
 #pragma unroll
-    for (int q = 0; q < kRankPer; ++q) {
-      if (x[q] >= tv) {  // rare: the exact test in key order
-        const uint32_t k = order_key(x[q]), i = id_of(c0, q);
-        if (k != 0u && (k > tk || (k == tk && i <= ti))) {
-          const int slot = atomicAdd(&s_ncand, 1);
-          if (slot < NS_MAX_SELECT_K + kMaxCand) {
-            cand_k[slot] = k;
-            cand_i[slot] = i;
-          } else {  // cannot happen: at most K * kRankPer values reach T
-            set_flag(err, NS_FLAG_INTERNAL | (4u << 8));
+    for (int g = 0; g < kRankPer / 4; ++g) {
+      // one compare per group of four (fmaxf skips NaN; padding is NaN), then per value
+      if (fmaxf(fmaxf(x[4 * g], x[4 * g + 1]), fmaxf(x[4 * g + 2], x[4 * g + 3])) >= tv) {
+#pragma unroll
+        for (int q = 4 * g; q < 4 * g + 4; ++q) {
+          if (x[q] >= tv) {  // rare: the exact test in key order
+            const uint32_t k = order_key(x[q]), i = id_of(c0, q);
+            if (k != 0u && (k > tk || (k == tk && i <= ti))) {
+              const int slot = atomicAdd(&s_ncand, 1);
+              if (slot < NS_MAX_SELECT_K + kMaxCand) {
+                cand_k[slot] = k;
+                cand_i[slot] = i;
+              } else {  // cannot happen: at most K * kRankPer values reach T
+                set_flag(err, NS_FLAG_INTERNAL | (4u << 8));
+              }
+            }
           }
         }
       }

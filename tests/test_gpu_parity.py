@@ -171,6 +171,53 @@ def test_empty_tree_and_reinit(pkg):
             check_state(h, 0, ost)
 
 
+def _special_rows(V, base):
+    """Verify rows that exercise the ranking order: NaN never ranks, -0.0 ties
+    +0.0, infinities are ordered, ties go to the smaller id, the best values
+    sit in the last (ragged) slots."""
+    rows = {}
+    r = base.copy()
+    r[[V - 1, V - 2, V - 3]] = [100.0, 99.0, 98.0]
+    rows["best_at_the_end"] = r
+    r = base.copy()
+    r[np.argsort(-base, kind="stable")[:5]] = np.nan
+    r[::97] = np.nan
+    rows["nan_where_the_best_was"] = r
+    r = -np.abs(base)
+    r[[7, 3, V - 2, 11]] = [-0.0, 0.0, 0.0, -0.0]
+    rows["signed_zero_ties"] = r
+    rows["all_equal"] = np.full(V, 1.5, np.float32)
+    r = np.full(V, -np.inf, np.float32)
+    r[[V // 2, 9]] = [-3.0, 2.0]
+    rows["minus_inf_fill"] = r
+    r = base.copy()
+    r[V // 3] = np.inf
+    rows["plus_inf"] = r
+    rows["all_nan"] = np.full(V, np.nan, np.float32)
+    return rows
+
+
+@pytest.mark.parametrize("V", [4099, 4100], ids=["scalar", "float4"])
+def test_verify_rows_with_special_values(pkg, V):
+    cfg = WorkloadConfig(name=f"special{V}", V=V, H=64, W_max=64, K_pre=2, K_ver=3, prompt_len=12, self_copy=0.2,
+                         zipf_s=1.1, steps=1, n_tree=8, tree_local=0.5, tree_recent=8, n_verify=1)
+    wl = Workload(cfg)
+    prompt, Z, tree = wl.prompt(0), wl.prefill_logits(0), wl.trees(0)[0]
+    with _handle(pkg, cfg, max_prompt=64) as h:
+        for name, row in _special_rows(V, wl.verify_logits(0, 0)[0]).items():
+            ost = oracle.OracleStream(cfg.V, cfg.W_max, cfg.K_pre, cfg.K_ver)
+            ost.init(prompt, Z)
+            h.stream_init(0, dev_i32(prompt), dev_f32(Z))
+            h.stream_append(0, dev_i32(tree), dev_f32(row[None, :]), 0)
+            h.build_active_vocab(0)
+            ost.append(tree, row[None, :], 0)
+            check_state(h, 0, ost)
+            flags = h.get_error(clear=True)
+            short = len(oracle.top_k(row, cfg.K_ver)) < cfg.K_ver
+            assert bool(flags & pkg.FLAG_BAD_ID) == short, name
+            assert flags & ~pkg.FLAG_BAD_ID == 0, name
+
+
 def test_bad_ids_are_skipped_and_flagged(pkg):
     cfg = WorkloadConfig(name="bad", V=500, H=64, W_max=40, K_pre=2, K_ver=2, prompt_len=30, self_copy=0.2,
                          zipf_s=1.0, steps=1, n_tree=10, tree_local=0.5, tree_recent=8, n_verify=1)
