@@ -63,16 +63,13 @@ __device__ int block_exclusive_scan(int v, int *sh, int *total) {
 //  ids of a sparse word itself; the lanes of a warp write a dense word's ids
 //  together, one bit each.
 // Most words are zero when |I_t| << V; only the listed ones cost work after
-// the scan.  With `stage` (shared, W_max ints) the ids are gathered there and
-// copied to `active` with coalesced stores; without it they go straight to
-// `active`.
+// the scan.
 constexpr int kCompactMaxG = 4;   // groups of four words per thread (V <= 4 * 4 * 1024 * 32)
 constexpr int kDenseBits = 8;     // a word with more set bits is emitted by its whole warp
-constexpr int kStageMaxW = 8192;  // largest W_max whose I_t is staged in shared memory
 static_assert(kStateThreads == kWarp * kWarp, "the block scan takes one warp of warp totals");
 
 __device__ void compact_bitmap(const uint32_t *bits, int nwords, int nwords_pad, int32_t *nz_w, int32_t *nz_o,
-                               int32_t *stage, int32_t *active, int32_t *count, int W_max, uint32_t *err,
+                               int32_t *active, int32_t *count, int W_max, uint32_t *err,
                                int *sh /* 2 * kWarp ints */) {
   const int T = kStateThreads, tid = threadIdx.x;
   const int lane = tid & (kWarp - 1), warp = tid / kWarp;
@@ -138,7 +135,7 @@ __device__ void compact_bitmap(const uint32_t *bits, int nwords, int nwords_pad,
     }
   }
   __syncthreads();
-  int32_t *out = stage != nullptr ? stage : active;
+  int32_t *out = active;
   const uint32_t lt = (1u << lane) - 1u;
   for (int r = 0; r * T < n_nz; ++r) {
     const int k = r * T + kWarp * lane + ((warp + lane) & (kWarp - 1));
@@ -170,10 +167,6 @@ __device__ void compact_bitmap(const uint32_t *bits, int nwords, int nwords_pad,
     }
   }
   const int n = total < W_max ? total : W_max;
-  if (stage != nullptr) {
-    __syncthreads();
-    for (int j = tid; j < n; j += T) active[j] = stage[j];
-  }
   if (tid == 0) {
     if (total > W_max) set_flag(err, NS_FLAG_OVERFLOW);
     *count = n;
@@ -181,10 +174,8 @@ __device__ void compact_bitmap(const uint32_t *bits, int nwords, int nwords_pad,
 }
 
 // Dynamic shared memory of the state kernels, in words: the bitmap, the list
-// of nonzero words and their offsets, then (when W_max allows) the staged I_t.
-__host__ __device__ inline int state_smem_words(int nwords_pad, int W_max) {
-  return 3 * nwords_pad + (W_max <= kStageMaxW ? ((W_max + 3) & ~3) : 0);
-}
+// of nonzero words and their offsets.
+__host__ __device__ inline int state_smem_words(int nwords_pad) { return 3 * nwords_pad; }
 
 // ---------------------------------------------------------------------------
 // Prefill initialisation (per request)
@@ -327,7 +318,7 @@ constexpr int kHashSlots = 256;                        // >= the most distinct i
 
 template <bool VEC, bool BUILD>
 __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims d, const int32_t *tree, int n_tree, const float *zrow, uint32_t *err) {
-  extern __shared__ uint4 s_dyn4[];  // leader: the bitmap, the nonzero-word list (nwords_pad words each), the staged I_t
+  extern __shared__ uint4 s_dyn4[];  // leader: the bitmap and the nonzero-word list (nwords_pad words each)
   __shared__ uint32_t wl_k[kStateWarps * NS_MAX_SELECT_K], wl_i[kStateWarps * NS_MAX_SELECT_K];
   __shared__ uint32_t cand_k[NS_MAX_SELECT_K + kMaxCand], cand_i[NS_MAX_SELECT_K + kMaxCand];
   __shared__ uint32_t res_k[NS_MAX_SELECT_K], res_i[NS_MAX_SELECT_K];
@@ -356,7 +347,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
   uint32_t *s_bits = reinterpret_cast<uint32_t *>(s_dyn4);
   int32_t *s_nzw = reinterpret_cast<int32_t *>(s_bits + d.nwords_pad);
   int32_t *s_nzo = s_nzw + d.nwords_pad;
-  int32_t *s_stage = d.W_max <= kStageMaxW ? s_nzo + d.nwords_pad : nullptr;
 
   // ---- leader: the bitmap starts streaming into shared memory -------------
   if (leader && tid == 0) {
@@ -700,20 +690,19 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
   __syncthreads();
 
   if (BUILD && have_bits)
-    compact_bitmap(s_bits, d.nwords, d.nwords_pad, s_nzw, s_nzo, s_stage, s.active, s.count, d.W_max, err, sh_scan);
+    compact_bitmap(s_bits, d.nwords, d.nwords_pad, s_nzw, s_nzo, s.active, s.count, d.W_max, err, sh_scan);
 }
 
 __global__ void __launch_bounds__(kStateThreads) build_kernel(SeqDev s, Dims d, uint32_t *err) {
-  extern __shared__ uint4 s_dyn4[];  // the bitmap, the nonzero-word list (nwords_pad words each), the staged I_t
+  extern __shared__ uint4 s_dyn4[];  // the bitmap and the nonzero-word list (nwords_pad words each)
   __shared__ int sh_scan[2 * kWarp];
   uint32_t *s_bits = reinterpret_cast<uint32_t *>(s_dyn4);
   int32_t *s_nzw = reinterpret_cast<int32_t *>(s_bits + d.nwords_pad);
   int32_t *s_nzo = s_nzw + d.nwords_pad;
-  int32_t *s_stage = d.W_max <= kStageMaxW ? s_nzo + d.nwords_pad : nullptr;
   const uint4 *g4 = reinterpret_cast<const uint4 *>(s.bitmap);
   for (int q = threadIdx.x; q < d.nwords_pad / 4; q += blockDim.x) s_dyn4[q] = g4[q];
   __syncthreads();
-  compact_bitmap(s_bits, d.nwords, d.nwords_pad, s_nzw, s_nzo, s_stage, s.active, s.count, d.W_max, err, sh_scan);
+  compact_bitmap(s_bits, d.nwords, d.nwords_pad, s_nzw, s_nzo, s.active, s.count, d.W_max, err, sh_scan);
 }
 
 // packed[j, :] = W[I_t[j], :]; each CTA copies 4 rows per iteration with all
@@ -766,7 +755,7 @@ cudaError_t launch_append_k(const SeqDev &s, const Dims &d, const int32_t *tree,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d.state_cluster, 1, 1);
   cfg.blockDim = dim3(kStateThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)state_smem_words(d.nwords_pad, d.W_max) * 4;
+  cfg.dynamicSmemBytes = (size_t)state_smem_words(d.nwords_pad) * 4;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -839,7 +828,7 @@ cudaError_t launch_init(const SeqDev &s, const Dims &d, const int32_t *prompt, i
 }
 
 cudaError_t prepare_state_kernels(Dims *d) {
-  const int bytes = state_smem_words(d->nwords_pad, d->W_max) * 4;
+  const int bytes = state_smem_words(d->nwords_pad) * 4;
   cudaError_t e = cudaSuccess;
   const cudaError_t r[] = {allow_append<true, true>(bytes), allow_append<true, false>(bytes),
                            allow_append<false, true>(bytes), allow_append<false, false>(bytes),
@@ -863,7 +852,7 @@ cudaError_t launch_append(const SeqDev &s, const Dims &d, const int32_t *tree, i
 }
 
 cudaError_t launch_build(const SeqDev &s, const Dims &d, uint32_t *err, cudaStream_t st) {
-  build_kernel<<<1, kStateThreads, (size_t)state_smem_words(d.nwords_pad, d.W_max) * 4, st>>>(s, d, err);
+  build_kernel<<<1, kStateThreads, (size_t)state_smem_words(d.nwords_pad) * 4, st>>>(s, d, err);
   return cudaGetLastError();
 }
 
