@@ -515,9 +515,11 @@ bool encode_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t ou
 
 int umma_tiles(int W_max) { return (W_max + kUM - 1) / kUM; }
 // Clusters of 16 CTAs halve each CTA's share of H (a shorter gather chain),
-// so they are used wherever the device holds them.  The grid has one
-// cluster per tile of W_max, capped at the clusters that are resident at
-// once; a cluster loops over tiles when |I_t| needs more.
+// but far fewer of them are resident at once than clusters of 8, and a tile
+// that waits for a second wave costs more than the halved chain saves.  So a
+// launch uses 16 only when every tile of W_max gets a resident cluster (by
+// the occupancy query), else 8.  The grid has one cluster per tile of W_max;
+// the kernel's tile loop also covers a grid of fewer clusters.
 int g_max16 = 0, g_max8 = 0;  // resident clusters of each size, from prepare_umma_kernels
 
 int umma_cluster() { return 16; }  // the most row slices a launch can use
@@ -579,10 +581,8 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   a.out_vals = L.out_vals;
   a.err = L.err;
   cudaLaunchConfig_t cfg = {};
-  const int CL = g_max16 > 0 ? 16 : 8;
-  const int resident = CL == 16 ? g_max16 : g_max8;
-  const int ncl = umma_tiles(L.W_max) < resident ? umma_tiles(L.W_max) : resident;
-  cfg.gridDim = dim3((unsigned)(ncl * CL));
+  const int CL = umma_tiles(L.W_max) <= g_max16 || g_max8 == 0 ? 16 : 8;
+  cfg.gridDim = dim3((unsigned)(umma_tiles(L.W_max) * CL));
   cfg.blockDim = dim3(kUThreads);
   cfg.dynamicSmemBytes = kUSmem;
   cfg.stream = st;
