@@ -214,8 +214,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * dt / done, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.name, "V": cfg.V, "H": cfg.H, "W_max": cfg.W_max, "n_tree": cfg.n_tree,
-                   "k": cfg.k},
+        "config": {"workload": cfg.name, "V": cfg.V, "H": cfg.H, "W_max": cfg.W_max, "K_pre": cfg.K_pre,
+                   "K_ver": cfg.K_ver, "n_tree": cfg.n_tree, "k": cfg.k, "parallelism": "replicas x1"},
         "cpu_baseline": {"value": v, "unit": "steps/s", "cores": cores, "kind": "oracle",
                          "sample": f"first {done} decode steps of {cfg.name} after its prefill init"},
         "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

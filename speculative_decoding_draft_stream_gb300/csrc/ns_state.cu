@@ -12,8 +12,6 @@
 // occurrences of id among those entries, and bitmap bit id is counts[id] > 0,
 // i.e. id in Unique(Suffix(S, W_max)).  Appending entry p overwrites the slot
 // of entry p - W_max, which is exactly the entry that leaves the window.
-#include <mutex>
-
 #include "ns_internal.cuh"
 #include "ns_ptx.cuh"
 
@@ -176,68 +174,8 @@ __device__ void compact_bitmap(const uint32_t *bits, int nwords, int nwords_pad,
 }
 
 // Dynamic shared memory of the state kernels, in words: the bitmap, the list
-// of nonzero words and their offsets, then (when W_max allows) the previous
-// I_t for the incremental update.
-constexpr int kIncMaxW = 8192;  // largest W_max whose I_t is updated in place of a recompaction
-__host__ __device__ inline int state_smem_words(int nwords_pad, int W_max) {
-  return 3 * nwords_pad + (W_max <= kIncMaxW ? ((W_max + 3) & ~3) : 0);
-}
-
-// The number of entries of the ascending array a[0, n) below x.
-__device__ __forceinline__ int count_below(const int32_t *a, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (a[mid] < x) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
-}
-
-// I_t after a step, from the I_t before it (fresh: it matched the bitmap)
-// and the ids whose bit was set (fa, na) or cleared (fr, nr) by the step:
-// (old minus cleared) plus set, ascending.  An old id keeps its rank minus
-// the cleared ids below it plus the set ids below it; a set id goes after
-// the surviving old ids below it and the set ids below it.  The set and
-// cleared lists are sorted here (ids are distinct within each); sa and sr
-// are shared scratch of na and nr ints.
-__device__ void update_active(const int32_t *old, int m_old, const int32_t *fa, int na, const int32_t *fr, int nr,
-                              int32_t *sa, int32_t *sr, int32_t *active, int32_t *count, int W_max, uint32_t *err) {
-  const int tid = threadIdx.x;
-  if (tid < na) {  // rank by counting
-    const int x = fa[tid];
-    int r = 0;
-    for (int j = 0; j < na; ++j) r += fa[j] < x;
-    sa[r] = x;
-  } else if (tid >= 128 && tid < 128 + nr) {
-    const int x = fr[tid - 128];
-    int r = 0;
-    for (int j = 0; j < nr; ++j) r += fr[j] < x;
-    sr[r] = x;
-  }
-  __syncthreads();
-  if (tid < na) {
-    const int x = sa[tid];
-    const int p = count_below(old, m_old, x) - count_below(sr, nr, x) + tid;
-    if ((unsigned)p < (unsigned)W_max) active[p] = x;
-  }
-  for (int q = 0; q < kIncMaxW / kStateThreads; ++q) {  // this thread's old ids
-    const int j = tid + q * kStateThreads;
-    if (j < m_old) {
-      const int a = old[j];
-      const int r = count_below(sr, nr, a);
-      if (!(r < nr && sr[r] == a)) {  // still in the window
-        const int p = j - r + count_below(sa, na, a);
-        if ((unsigned)p < (unsigned)W_max) active[p] = a;
-      }
-    }
-  }
-  if (tid == 0) {
-    const int m = m_old - nr + na;
-    if (m < 0 || m > W_max) set_flag(err, NS_FLAG_OVERFLOW);
-    *count = m < 0 ? 0 : (m < W_max ? m : W_max);
-  }
-}
+// of nonzero words and their offsets.
+__host__ __device__ inline int state_smem_words(int nwords_pad) { return 3 * nwords_pad; }
 
 // ---------------------------------------------------------------------------
 // Prefill initialisation (per request)
@@ -396,11 +334,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
   __shared__ uint32_t h_old[kHashSlots];
   __shared__ int s_misc[4];
   __shared__ long long s_len;
-  __shared__ int s_head;   // |S| mod W_max
-  __shared__ int s_fresh;  // I_t matches the bitmap before this step
-  __shared__ int s_mold;   // |I_t| before this step
-  __shared__ int s_nfa, s_nfr;  // ids whose window bit this step sets / clears
-  __shared__ int32_t s_fa[kMaxAppend], s_fr[kMaxAppend], s_sa[kMaxAppend], s_sr[kMaxAppend];
+  __shared__ int s_head;  // |S| mod W_max
   __shared__ __align__(8) unsigned long long s_bar;  // the bitmap copy
   __shared__ int sh_scan[2 * kWarp];
 
@@ -413,7 +347,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
   uint32_t *s_bits = reinterpret_cast<uint32_t *>(s_dyn4);
   int32_t *s_nzw = reinterpret_cast<int32_t *>(s_bits + d.nwords_pad);
   int32_t *s_nzo = s_nzw + d.nwords_pad;
-  int32_t *s_old = d.W_max <= kIncMaxW ? s_nzo + d.nwords_pad : nullptr;  // BUILD: I_t before this step
 
   // ---- leader: the bitmap starts streaming into shared memory -------------
   if (leader && tid == 0) {
@@ -480,19 +413,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
     if (tid == 0) {  // |S| and the ring slot of the next entry, one 16-byte load
       const longlong2 lv = *reinterpret_cast<const longlong2 *>(s.length);
       s_len = lv.x;
-      s_head = (int)(lv.y & 0xffffffffLL);
-      s_fresh = (int)(lv.y >> 32);
-      s_nfa = 0;
-      s_nfr = 0;
+      s_head = (int)lv.y;
     }
     if (tid < n_tree) s_tree[tid] = tree[tid];
     for (int q = tid; q < kHashSlots; q += blockDim.x) {
       h_key[q] = -1;
       h_dl[q] = 0;
-    }
-    if (BUILD && s_old != nullptr) {  // the leader ranks nothing: these loads cost it no time
-      if (tid == 1) s_mold = *s.count;
-      for (int q = tid; q < d.W_max; q += blockDim.x) s_old[q] = s.active[q];
     }
   }
   if (tid < K) {  // the running Top-K starts empty
@@ -730,13 +656,13 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
     const int off = (int)(ap_begin - len0) + tid;
     s.ring[(s_head + off) % W] = s_app[off];
   }
+  if (tid == 0) {
+    s.length[0] = len1;
+    s.length[1] = (s_head + m) % W;
+  }
   // The bitmap copy must have landed before its bits are read.  If the wait
   // gave up (NS_FLAG_TIMEOUT), the bitmap and I_t are left as they were.
   const bool have_bits = __syncthreads_and(mbar_wait(smem_u32(&s_bar), 0, err));
-  if (tid == 0) {  // |S|, the ring slot of the next entry, and whether I_t will match the bitmap
-    s.length[0] = len1;
-    s.length[1] = (long long)((s_head + m) % W) | (BUILD && have_bits ? (1LL << 32) : 0LL);
-  }
   // One thread per distinct id.  A net gain sets the bit of an id that was
   // outside the window (bit clear: count 0); a net loss happens only to an
   // evicted id, whose count was read above, and clears the bit when the
@@ -750,7 +676,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
         if (have_bits && !(s_bits[id >> 5] & bit)) {
           atomicOr(&s_bits[id >> 5], bit);
           atomicOr(&s.bitmap[id >> 5], bit);
-          s_fa[atomicAdd(&s_nfa, 1)] = id;  // distinct ids: at most kMaxAppend enter
         }
       } else {
         const long long now = (long long)h_old[tid] + net;
@@ -758,21 +683,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
         if (now == 0 && have_bits) {
           atomicAnd(&s_bits[id >> 5], ~bit);
           atomicAnd(&s.bitmap[id >> 5], ~bit);
-          s_fr[atomicAdd(&s_nfr, 1)] = id;  // distinct evicted ids: at most kMaxAppend leave
         }
       }
     }
   }
   __syncthreads();
 
-  if (BUILD && have_bits) {
-    // I_t: updated from the previous one when that matched the bitmap (the
-    // few ids that entered or left are merged in), else compacted anew.
-    if (s_old != nullptr && s_fresh && s_mold >= 0 && s_mold <= d.W_max)
-      update_active(s_old, s_mold, s_fa, s_nfa, s_fr, s_nfr, s_sa, s_sr, s.active, s.count, d.W_max, err);
-    else
-      compact_bitmap(s_bits, d.nwords, d.nwords_pad, s_nzw, s_nzo, s.active, s.count, d.W_max, err, sh_scan);
-  }
+  if (BUILD && have_bits)
+    compact_bitmap(s_bits, d.nwords, d.nwords_pad, s_nzw, s_nzo, s.active, s.count, d.W_max, err, sh_scan);
 }
 
 __global__ void __launch_bounds__(kStateThreads) build_kernel(SeqDev s, Dims d, uint32_t *err) {
@@ -785,7 +703,6 @@ __global__ void __launch_bounds__(kStateThreads) build_kernel(SeqDev s, Dims d, 
   for (int q = threadIdx.x; q < d.nwords_pad / 4; q += blockDim.x) s_dyn4[q] = g4[q];
   __syncthreads();
   compact_bitmap(s_bits, d.nwords, d.nwords_pad, s_nzw, s_nzo, s.active, s.count, d.W_max, err, sh_scan);
-  if (threadIdx.x == 0) s.length[1] = (s.length[1] & 0xffffffffLL) | (1LL << 32);  // I_t matches the bitmap
 }
 
 // packed[j, :] = W[I_t[j], :]; each CTA copies 4 rows per iteration with all
@@ -838,7 +755,7 @@ cudaError_t launch_append_k(const SeqDev &s, const Dims &d, const int32_t *tree,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d.state_cluster, 1, 1);
   cfg.blockDim = dim3(kStateThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)state_smem_words(d.nwords_pad, d.W_max) * 4;
+  cfg.dynamicSmemBytes = (size_t)state_smem_words(d.nwords_pad) * 4;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -911,12 +828,7 @@ cudaError_t launch_init(const SeqDev &s, const Dims &d, const int32_t *prompt, i
 }
 
 cudaError_t prepare_state_kernels(Dims *d) {
-  // The limit is a property of the kernel, shared by every handle: only raise it.
-  static std::mutex mu;
-  static int max_bytes = 0;
-  std::lock_guard<std::mutex> lock(mu);
-  const int need = state_smem_words(d->nwords_pad, d->W_max) * 4;
-  const int bytes = need > max_bytes ? need : max_bytes;
+  const int bytes = state_smem_words(d->nwords_pad) * 4;
   cudaError_t e = cudaSuccess;
   const cudaError_t r[] = {allow_append<true, true>(bytes), allow_append<true, false>(bytes),
                            allow_append<false, true>(bytes), allow_append<false, false>(bytes),
@@ -924,9 +836,8 @@ cudaError_t prepare_state_kernels(Dims *d) {
   for (cudaError_t x : r)
     if (x != cudaSuccess) e = x;
   if (e != cudaSuccess) return e;
-  max_bytes = bytes;
-  d->state_cluster = cluster_fits(kMaxStateCluster, need) ? kMaxStateCluster : 8;
-  return cluster_fits(d->state_cluster, need) ? cudaSuccess : cudaErrorNotSupported;
+  d->state_cluster = cluster_fits(kMaxStateCluster, bytes) ? kMaxStateCluster : 8;
+  return cluster_fits(d->state_cluster, bytes) ? cudaSuccess : cudaErrorNotSupported;
 }
 
 cudaError_t launch_append(const SeqDev &s, const Dims &d, const int32_t *tree, int n_tree, const float *zrow,
@@ -941,7 +852,7 @@ cudaError_t launch_append(const SeqDev &s, const Dims &d, const int32_t *tree, i
 }
 
 cudaError_t launch_build(const SeqDev &s, const Dims &d, uint32_t *err, cudaStream_t st) {
-  build_kernel<<<1, kStateThreads, (size_t)state_smem_words(d.nwords_pad, d.W_max) * 4, st>>>(s, d, err);
+  build_kernel<<<1, kStateThreads, (size_t)state_smem_words(d.nwords_pad) * 4, st>>>(s, d, err);
   return cudaGetLastError();
 }
 

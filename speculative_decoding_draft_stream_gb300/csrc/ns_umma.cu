@@ -336,9 +336,8 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
         ++released;
       }
     }
-    bulk_wait_read_all();
+    bulk_wait_read_all();  // the ring may be reused; the global writes finish in the background
     for (; released < nk; ++released) mbar_arrive(bar_empty + 8 * ((iter * nk + released) % kUStages));
-    bulk_wait_all();
   }
 
   // ---- epilogue: accumulator -> partial tile in shared memory ---------------
@@ -477,6 +476,7 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
   __syncwarp();
   cluster_sync();  // peers may still be reading this CTA's partial tile
   }  // tiles
+  if (warp == 2 && lane == 0) bulk_wait_all();  // the packed-buffer stores are complete before the CTA leaves
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
