@@ -245,11 +245,12 @@ def run_ours(args):
 
     nsbuild.build()
     import speculative_decoding_draft_stream_gb300 as ns
+    from speculative_decoding_draft_stream_gb300 import replicas
     from synth import Workload, get_config
 
     cfg = get_config(args.workload)
     wl = Workload(cfg)
-    seq = rank  # replicas: every rank decodes its own sequence
+    (seq,) = replicas.rank_sequences(rank, world)  # replicas: every rank decodes its own sequence
     n, H, V, k = cfg.n_tree, cfg.H, cfg.V, cfg.k
     T = min(cfg.steps, args.decode_steps) if args.decode_steps > 0 else cfg.steps
 
@@ -288,11 +289,7 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     def max_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return replicas.max_over_ranks(x, dist, dev)
 
     clocks = ClockSampler(local if world > 1 else None)
     clocks.start()
@@ -352,7 +349,7 @@ def run_ours(args):
         raise RuntimeError("device error flags set during the timed steps")
     diffs = sorted(x - y for x, y in rounds)
     total_ms = max_over_ranks(diffs[len(diffs) // 2])  # median of three
-    steps_per_s = world * K / (total_ms / 1e3)
+    steps_per_s = replicas.whole_job_rate(K, world, total_ms / 1e3)
     del g_steps, g_flush
 
     # ---- per-kernel breakdown: the same K steps with ns_step's trace events ---
@@ -426,7 +423,7 @@ def run_ours(args):
         e2e_s += time.perf_counter() - t0
     barrier()
     e2e_s = max_over_ranks(e2e_s)
-    e2e = world * K / e2e_s
+    e2e = replicas.whole_job_rate(K, world, e2e_s)
 
     # ---- extras: the |I_t|~3k point and the dense heads ----------------------
     # Each is timed as (graph of R x [flush + op]) - (graph of R x [flush]).
