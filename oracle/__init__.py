@@ -13,6 +13,7 @@ No function here is "parity unpinned".
 """
 
 from .nanospec_oracle import (  # noqa: F401
+    OracleSlots,
     OracleStream,
     active_vocab,
     bf16_to_f64,
@@ -21,6 +22,10 @@ from .nanospec_oracle import (  # noqa: F401
     draft_candidates,
     gather_rows,
     project,
+    slot_gather,
+    slot_high_water,
+    slot_project_topk,
+    slot_update,
     stream_append,
     stream_init,
     sub_head_step,

@@ -26,6 +26,9 @@ MicroSpec; section numbers are MicroSpec's, which keeps its headings):
             product.
 * [bitmap]  MicroSpec §3.3 "Eliminating Overhead via GPU-Resident State
             Management": the active window kept as bitmaps.
+* [slots]   NanoSpec, "Avoiding Sparse Computation via Asynchronous
+            Gathering": the weights of newly active tokens are gathered into
+            the pre-allocated contiguous buffer.
 
 Readings where the pages are silent (each also listed in the design notes):
 
@@ -47,6 +50,12 @@ Readings where the pages are silent (each also listed in the design notes):
    rounded once to fp32.
 9. Top-k of a row with fewer than k active columns is padded with id -1 and
    value -inf.
+10. Slot-stable buffer (the incremental reading of [gather]: only the rows of
+   newly active tokens are gathered).  The pages fix no slot rule; here a
+   slot whose id left I_t is freed, and the ids of I_t that hold no slot take
+   the free slots in ascending id order, lowest slot first.  The first update
+   after the stream is initialised therefore lays I_1 out ascending, the same
+   layout as the full repack.
 
 """
 
@@ -239,6 +248,84 @@ def sub_head_step(hid_bits, W_bits, I, k: int):
     logits = project(hid_bits, packed)
     ids, vals = topk_remap(logits, I, k)
     return packed, logits, ids, vals
+
+
+# ---------------------------------------------------------------------------
+# Slot-stable packed buffer [slots] (reading 10)
+# ---------------------------------------------------------------------------
+def slot_update(slot_id, I):
+    """One update of the slot table to the active set I.
+
+    ``slot_id`` has one entry per buffer slot (W_max of them): the id held,
+    or -1 for a free slot.  Returns (new table, new_pairs): every slot whose
+    id is not in I is freed; then the ids of I that hold no slot, ascending,
+    take the free slots, lowest slot first.  ``new_pairs`` lists the
+    (slot, id) assignments made, in that order; they are the rows to gather.
+    """
+    table = [int(x) for x in slot_id]
+    active = set(int(x) for x in I)
+    if len(active) > len(table):
+        raise ValueError("more active ids than slots")
+    for sl, x in enumerate(table):
+        if x >= 0 and x not in active:
+            table[sl] = -1
+    held = set(x for x in table if x >= 0)
+    new_ids = sorted(active - held)
+    free = [sl for sl, x in enumerate(table) if x < 0]
+    pairs = list(zip(free, new_ids))
+    for sl, x in pairs:
+        table[sl] = x
+    return np.array(table, dtype=np.int32), pairs
+
+
+def slot_high_water(slot_id) -> int:
+    """One past the highest occupied slot (0 for an empty table)."""
+    occ = np.flatnonzero(np.asarray(slot_id) >= 0)
+    return int(occ[-1]) + 1 if len(occ) else 0
+
+
+def slot_gather(rows_bits, W_bits, pairs) -> np.ndarray:
+    """The buffer after copying W_head[id, :] into slot ``slot`` for every
+    (slot, id) in ``pairs``; every other slot keeps its bytes."""
+    out = np.array(rows_bits, dtype=np.uint16, copy=True)
+    W_bits = np.asarray(W_bits, dtype=np.uint16)
+    for sl, x in pairs:
+        out[sl] = W_bits[x]
+    return out
+
+
+def slot_project_topk(hid_bits, rows_bits, slot_id, k: int):
+    """Projection over the slot buffer and per-row top-k of the occupied slots.
+
+    Returns (logits fp32 [n, hw], ids, vals): logits[r, s] = Eq. 1 over slot
+    s's row for s < hw (free slots included, unranked); the top-k ranks only
+    occupied slots, maps them to the ids they hold and orders by value, then
+    the smaller id, exactly as the full repack does (its columns are the ids
+    in ascending order).
+    """
+    slot_id = np.asarray(slot_id, dtype=np.int64)
+    hw = slot_high_water(slot_id)
+    logits = project(hid_bits, np.asarray(rows_bits)[:hw])
+    occ = np.flatnonzero(slot_id[:hw] >= 0)
+    by_id = occ[np.argsort(slot_id[occ], kind="stable")]  # occupied slots, ids ascending
+    ids, vals = topk_remap(logits[:, by_id], slot_id[by_id], k)
+    return logits, ids, vals
+
+
+class OracleSlots:
+    """The slot table and buffer of one sequence."""
+
+    def __init__(self, W_max: int, H: int):
+        self.slot_id = np.full(W_max, -1, dtype=np.int32)
+        self.rows = np.zeros((W_max, H), dtype=np.uint16)
+
+    def update(self, I, W_bits):
+        self.slot_id, pairs = slot_update(self.slot_id, I)
+        self.rows = slot_gather(self.rows, W_bits, pairs)
+        return pairs
+
+    def project_topk(self, hid_bits, k: int):
+        return slot_project_topk(hid_bits, self.rows, self.slot_id, k)
 
 
 # ---------------------------------------------------------------------------
