@@ -452,6 +452,56 @@ def run_ours(args):
                 out.append(a.elapsed_time(b))
             return 1e3 * min(out[0] - out[1], out[2] - out[3]) / reps
 
+        # the slot-stable buffer: K steps of ns_step_slots (state update, slot
+        # update + copy of the newly placed rows, projection over the slots),
+        # timed like the headline steps
+        def slot_step(t):
+            u = t % T
+            h.step_slots(0, trees_d[u], verify_d[u], vrows[u], W_d, hid_d[u], k, logits=logits, ids=ids, vals=vals)
+
+        def slot_graph(with_steps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for t in range(K):
+                    flush.zero_()
+                    if with_steps:
+                        slot_step(t)
+            return g
+
+        def slot_init():
+            init()
+            h.gather_new_head_rows(0, W_d)
+
+        slot_init()
+        for t in range(args.warmup):
+            slot_step(t)
+        torch.cuda.synchronize()
+        gs, gf = slot_graph(True), slot_graph(False)
+        sr = []
+        for _ in range(3):
+            slot_init()
+            barrier()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            gs.replay()
+            b.record()
+            barrier()
+            sr.append(a.elapsed_time(b) - replay_ms(gf, False))
+        del gs, gf
+        slot_init()
+        _, smeta, _, _, _ = h.get_slots(0)
+        copied = torch.zeros(K, dtype=torch.int32, device=dev)
+        for t in range(K):
+            slot_step(t)
+            copied[t:t + 1].copy_(smeta[1:2])
+        copied = copied.cpu().numpy()
+        if h.get_error() != 0:
+            raise RuntimeError("device error flags set during the slot-buffer steps")
+        us_slot = 1e3 * sorted(sr)[1] / K
+        extra["slot_step"] = {"us_per_step": us_slot, "rows_copied_mean": float(copied.mean()),
+                              "rows_copied_max": int(copied.max()), "mean_active": float(np.mean(m_list)),
+                              "vs_full_repack_step": (1e3 * total_ms / K) / us_slot}
+
         init()
         torch.cuda.synchronize()
         m0 = int(cnt.item())

@@ -209,6 +209,52 @@ NS_API ns_status ns_gather_sub_lm_head_topk(ns_handle *h, int32_t seq, const uin
                                             ns_stream stream);
 
 /*
+ * Slot-stable packed buffer: the incremental reading of NanoSpec's
+ * "Avoiding Sparse Computation via Asynchronous Gathering" (only the weights
+ * of newly active tokens are gathered into the pre-allocated contiguous
+ * buffer).  Each sequence has a second buffer of W_max row slots, separate
+ * from the packed buffer above, and a table of the id each slot holds.
+ *
+ * ns_gather_new_head_rows updates the table to the current I_t (the one the
+ * last ns_build_active_vocab / ns_state_update / ns_step produced) and copies
+ * only the rows of the ids it places: every slot whose id left I_t is freed;
+ * then the ids of I_t that hold no slot take the free slots in ascending id
+ * order, lowest slot first (the pages fix no rule; this is the one used).
+ * An id keeps its slot while it stays active.  ns_stream_init empties the
+ * table, so the first update after it lays I_1 out ascending (as the full
+ * repack does) and copies |I_1| rows; later updates copy |I_t \ I_{t-1}|.
+ * Meant for a copy stream like ns_gather_head_rows: `done` (nullable) is
+ * recorded on copy_stream after the copy.  d_W_head: bf16 [V x H].
+ */
+NS_API ns_status ns_gather_new_head_rows(ns_handle *h, int32_t seq, const uint16_t *d_W_head,
+                                         ns_stream copy_stream, ns_event done);
+
+/*
+ * Projection and top-k over the slot buffer (tcgen05):
+ *   logits[r, s] = sum_h hidden[r, h] * slot_row[s, h]  for s < high-water mark
+ * (one past the highest occupied slot; columns of free slots below it hold
+ * unspecified values and are never ranked), then per row the k largest logits
+ * of occupied slots mapped to the ids they hold, ties to the smaller id.  The
+ * ids and values equal those of ns_sub_lm_head_logits_topk on the same I_t;
+ * only the logits' column order differs (by slot instead of by position in
+ * I_t).  Arguments as ns_sub_lm_head_logits_topk (ld_logits >= W_max).
+ */
+NS_API ns_status ns_slot_lm_head_logits_topk(ns_handle *h, int32_t seq, const uint16_t *d_hidden, int32_t n,
+                                             int32_t k, float *d_logits, int32_t ld_logits, int32_t *d_topk_ids,
+                                             float *d_topk_vals, ns_stream stream);
+
+/*
+ * One decode step on the slot buffer: ns_state_update, ns_gather_new_head_rows
+ * and ns_slot_lm_head_logits_topk in order on `stream` (three kernels and the
+ * row copy).  Arguments as ns_step; the logits are indexed by slot.
+ */
+NS_API ns_status ns_step_slots(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
+                               const float *d_verify_logits, int32_t n_verify, int32_t verify_row,
+                               const uint16_t *d_W_head, const uint16_t *d_hidden, int32_t n, int32_t k,
+                               float *d_logits, int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
+                               ns_stream stream);
+
+/*
  * Per-kernel event trace (MicroSpec §4 profiles per-step latency with CUDA
  * event recording).  While set, ns_step records, on its stream,
  *   events[0] before its first kernel,
@@ -279,6 +325,18 @@ NS_API ns_status ns_get_active(ns_handle *h, int32_t seq, const int32_t **ids, c
  */
 NS_API ns_status ns_get_state(ns_handle *h, int32_t seq, const int32_t **ring, const int64_t **length,
                        const uint32_t **counts);
+
+/*
+ * Device pointers to a sequence's slot buffer (owned by the handle).  Any
+ * out-pointer may be NULL.
+ *   slot_id    int32 [W_max]  id held by each slot, -1 = free
+ *   meta       int32 [2]      high-water mark; rows copied by the last update
+ *   new_slots  int32 [W_max]  slots the last update filled (first meta[1] valid),
+ *   new_ids    int32 [W_max]  and the ids placed there, in ascending id order
+ *   rows       bf16 [W_max x H]  slot s holds W_head[slot_id[s], :] when occupied
+ */
+NS_API ns_status ns_get_slots(ns_handle *h, int32_t seq, const int32_t **slot_id, const int32_t **meta,
+                              const int32_t **new_slots, const int32_t **new_ids, const uint16_t **rows);
 
 /* Synchronises the device, returns the sticky NS_FLAG_* mask, and clears it
  * when `clear` is non-zero. */

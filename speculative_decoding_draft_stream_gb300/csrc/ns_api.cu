@@ -19,6 +19,7 @@ struct ns_handle {
   int num_sms = 0;
   int pgrid = 1;  // CTAs of the projection
   int ggrid = 1;  // CTAs of the gather
+  int sgrid = 1;  // CTAs of the slot-row copy
   char *base = nullptr;
   size_t bytes = 0;
   uint32_t *err = nullptr;
@@ -77,6 +78,12 @@ void layout(ns_handle *h, Carver &cv) {
     s.cand_k = cv.take<uint32_t>(ncand);
     s.cand_i = cv.take<uint32_t>(ncand);
     s.slice_ticket = cv.take<int32_t>(ns::umma_cluster());
+    s.slot_id = cv.take<int32_t>(c.W_max);
+    s.held = cv.take<uint32_t>(d.nwords_pad);
+    s.slot_meta = cv.take<int32_t>(2);
+    s.new_slot = cv.take<int32_t>(c.W_max);
+    s.new_id = cv.take<int32_t>(c.W_max);
+    s.slot_rows = cv.take<uint16_t>((size_t)c.W_max * c.H);
   }
   h->dense_ld = (c.V + 3) & ~3;
   h->dense_logits = cv.take<float>((size_t)ns::kProjBN * h->dense_ld);
@@ -131,12 +138,13 @@ ns_status ns_create(const ns_config *cfg, ns_handle **out) {
   d.nwords = (c.V + 31) / 32;
   d.nwords_pad = (d.nwords + 3) & ~3;
   d.ld_scratch = (c.W_max + 3) & ~3;
-  if (ns::prepare_state_kernels(&d) != cudaSuccess) {
+  if (ns::prepare_state_kernels(&d) != cudaSuccess || ns::prepare_slot_kernels(d) != cudaSuccess) {
     delete h;
     return NS_ERR_CUDA;
   }
   h->pgrid = 2 * h->num_sms;
   h->ggrid = 4 * h->num_sms;
+  h->sgrid = 2 * h->num_sms;
 
   Carver sizing(nullptr);
   layout(h, sizing);
@@ -282,18 +290,19 @@ static cudaError_t trace_record(cudaEvent_t ev, cudaStream_t st) {
 static cudaError_t enqueue_gather_project(ns_handle *h, int32_t seq, const uint16_t *d_W_head,
                                           const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
                                           int32_t ld_logits, int32_t *d_ids, float *d_vals, cudaStream_t cs,
-                                          cudaEvent_t mid, bool programmatic) {
+                                          cudaEvent_t mid, bool programmatic, bool slots = false) {
   const ns::SeqDev &s = h->seqs[seq];
   ns::UmmaLaunch L{};
-  L.W = d_W_head;
+  L.W = slots ? s.slot_rows : d_W_head;
   L.V = h->cfg.V;
   L.H = h->cfg.H;
   L.hid = d_hidden;
   L.n = n;
-  L.packed = s.packed;
+  L.packed = slots ? s.slot_rows : s.packed;
   L.W_max = h->cfg.W_max;
-  L.idx = s.active;
-  L.count_ptr = s.count;
+  L.idx = slots ? s.slot_id : s.active;
+  L.count_ptr = slots ? s.slot_meta : s.count;
+  L.slots = slots;
   L.k = k;
   L.logits = d_logits ? d_logits : s.logits;
   L.ld = d_logits ? ld_logits : h->dims.ld_scratch;
@@ -337,6 +346,45 @@ ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t 
     e = enqueue_gather_project(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals, cs,
                                tr ? h->trace[2] : nullptr, !tr);
   if (e == cudaSuccess && tr) e = trace_record(h->trace[3], cs);
+  return cuda_status(e);
+}
+
+ns_status ns_gather_new_head_rows(ns_handle *h, int32_t seq, const uint16_t *d_W_head, ns_stream copy_stream,
+                                  ns_event done) {
+  if (!valid_seq(h, seq) || !d_W_head || !aligned16(d_W_head)) return NS_ERR_ARG;
+  if (!h->inited[seq]) return NS_ERR_STATE;
+  cudaStream_t st = static_cast<cudaStream_t>(copy_stream);
+  cudaError_t e = ns::launch_slot_update(h->seqs[seq], h->dims, d_W_head, h->sgrid, h->err, st);
+  if (e == cudaSuccess && done) e = cudaEventRecord(static_cast<cudaEvent_t>(done), st);
+  return cuda_status(e);
+}
+
+ns_status ns_slot_lm_head_logits_topk(ns_handle *h, int32_t seq, const uint16_t *d_hidden, int32_t n, int32_t k,
+                                      float *d_logits, int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
+                                      ns_stream stream) {
+  if (!valid_seq(h, seq)) return NS_ERR_ARG;
+  ns_status st = check_proj_args(h, d_hidden, n, k, d_logits, ld_logits, h->cfg.W_max, d_topk_ids, d_topk_vals);
+  if (st != NS_OK) return st;
+  if (!h->inited[seq]) return NS_ERR_STATE;
+  return cuda_status(enqueue_gather_project(h, seq, nullptr, d_hidden, n, k, d_logits, ld_logits, d_topk_ids,
+                                            d_topk_vals, static_cast<cudaStream_t>(stream), nullptr, false, true));
+}
+
+ns_status ns_step_slots(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
+                        const float *d_verify_logits, int32_t n_verify, int32_t verify_row, const uint16_t *d_W_head,
+                        const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits, int32_t ld_logits,
+                        int32_t *d_topk_ids, float *d_topk_vals, ns_stream stream) {
+  ns_status st = check_append_args(h, seq, d_tree_ids, n_tree, d_verify_logits, n_verify, verify_row);
+  if (st != NS_OK) return st;
+  st = check_gather_project_args(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals);
+  if (st != NS_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
+  cudaError_t e = ns::launch_append(h->seqs[seq], h->dims, d_tree_ids, n_tree, zrow, true, h->err, cs);
+  if (e == cudaSuccess) e = ns::launch_slot_update(h->seqs[seq], h->dims, d_W_head, h->sgrid, h->err, cs);
+  if (e == cudaSuccess)
+    e = enqueue_gather_project(h, seq, nullptr, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals, cs,
+                               nullptr, true, true);
   return cuda_status(e);
 }
 
@@ -395,6 +443,18 @@ ns_status ns_get_state(ns_handle *h, int32_t seq, const int32_t **ring, const in
   if (ring) *ring = s.ring;
   if (length) *length = reinterpret_cast<const int64_t *>(s.length);
   if (counts) *counts = s.counts;
+  return NS_OK;
+}
+
+ns_status ns_get_slots(ns_handle *h, int32_t seq, const int32_t **slot_id, const int32_t **meta,
+                       const int32_t **new_slots, const int32_t **new_ids, const uint16_t **rows) {
+  if (!valid_seq(h, seq)) return NS_ERR_ARG;
+  const ns::SeqDev &s = h->seqs[seq];
+  if (slot_id) *slot_id = s.slot_id;
+  if (meta) *meta = s.slot_meta;
+  if (new_slots) *new_slots = s.new_slot;
+  if (new_ids) *new_ids = s.new_id;
+  if (rows) *rows = s.slot_rows;
   return NS_OK;
 }
 

@@ -41,6 +41,13 @@ struct SeqDev {
   uint32_t *cand_k;   // [umma tiles x 64 x max_k] per-tile top-k candidates (order keys)
   uint32_t *cand_i;
   int32_t *slice_ticket;  // [umma cluster] arrival counters of the row slices
+  // slot-stable buffer (incremental gather of the rows of newly active ids)
+  int32_t *slot_id;     // [W_max] id whose row slot s holds, -1 = free
+  uint32_t *held;       // [nwords_pad] bit id <=> id holds a slot (the window bitmap at the last slot update)
+  int32_t *slot_meta;   // [2] high-water mark (one past the highest occupied slot), rows the last update gathered
+  int32_t *new_slot;    // [W_max] (slot, id) of each row the last update gathered, in assignment order
+  int32_t *new_id;      // [W_max]
+  uint16_t *slot_rows;  // [W_max x H] bf16 slot buffer
 };
 
 struct Dims {
@@ -275,6 +282,37 @@ __device__ __forceinline__ void warp_select_keys(uint32_t *ck, uint32_t *ci, int
 
 __device__ __forceinline__ void set_flag(uint32_t *err, uint32_t f) { atomicOr(err, f); }
 
+__device__ __forceinline__ int warp_inclusive_scan(int v) {
+  const int lane = threadIdx.x & (kWarp - 1);
+#pragma unroll
+  for (int off = 1; off < kWarp; off <<= 1) {
+    int o = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += o;
+  }
+  return v;
+}
+
+// Exclusive prefix sum of one int per thread over the block.  `sh` needs
+// blockDim/32 ints.  Returns the exclusive prefix; *total gets the block sum.
+__device__ inline int block_exclusive_scan(int v, int *sh, int *total) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  const int warp = threadIdx.x / kWarp;
+  const int nwarps = blockDim.x / kWarp;
+  int incl = warp_inclusive_scan(v);
+  if (lane == kWarp - 1) sh[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int t = lane < nwarps ? sh[lane] : 0;
+    t = warp_inclusive_scan(t);
+    if (lane < nwarps) sh[lane] = t;
+  }
+  __syncthreads();
+  const int warp_off = warp > 0 ? sh[warp - 1] : 0;
+  *total = sh[nwarps - 1];
+  __syncthreads();
+  return warp_off + incl - v;
+}
+
 // ---------------------------------------------------------------------------
 // Launch wrappers (return cudaError_t of the launch).
 // ---------------------------------------------------------------------------
@@ -286,6 +324,12 @@ cudaError_t launch_append(const SeqDev &s, const Dims &d, const int32_t *tree, i
 cudaError_t prepare_state_kernels(Dims *d);
 cudaError_t launch_build(const SeqDev &s, const Dims &d, uint32_t *err, cudaStream_t st);
 cudaError_t launch_gather(const SeqDev &s, const Dims &d, const uint16_t *W, int grid, cudaStream_t st);
+
+// Slot-stable buffer (ns_slots.cu): update the slot table to I_t, then copy
+// the rows of the newly placed ids from W_head.
+cudaError_t prepare_slot_kernels(const Dims &d);
+cudaError_t launch_slot_update(const SeqDev &s, const Dims &d, const uint16_t *W, int copy_grid, uint32_t *err,
+                               cudaStream_t st);
 
 // Projection source modes.
 enum ProjMode { kFromPacked = 0, kGatherRows = 1, kDenseRows = 2 };
@@ -331,6 +375,7 @@ struct UmmaLaunch {
   float *out_vals;
   uint32_t *err;
   bool programmatic;         // may start while the preceding kernel finishes
+  bool slots;                // rows from the slot buffer (W = slot rows, idx = slot ids, count = high-water mark)
 };
 int umma_tiles(int W_max);
 int umma_cluster();

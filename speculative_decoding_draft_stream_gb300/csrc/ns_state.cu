@@ -20,37 +20,6 @@ namespace {
 
 constexpr int kMaxAppend = NS_MAX_ROWS + NS_MAX_SELECT_K;
 
-__device__ __forceinline__ int warp_inclusive_scan(int v) {
-  const int lane = threadIdx.x & (kWarp - 1);
-#pragma unroll
-  for (int off = 1; off < kWarp; off <<= 1) {
-    int o = __shfl_up_sync(0xffffffffu, v, off);
-    if (lane >= off) v += o;
-  }
-  return v;
-}
-
-// Exclusive prefix sum of one int per thread over the block.  `sh` needs
-// blockDim/32 ints.  Returns the exclusive prefix; *total gets the block sum.
-__device__ int block_exclusive_scan(int v, int *sh, int *total) {
-  const int lane = threadIdx.x & (kWarp - 1);
-  const int warp = threadIdx.x / kWarp;
-  const int nwarps = blockDim.x / kWarp;
-  int incl = warp_inclusive_scan(v);
-  if (lane == kWarp - 1) sh[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int t = lane < nwarps ? sh[lane] : 0;
-    t = warp_inclusive_scan(t);
-    if (lane < nwarps) sh[lane] = t;
-  }
-  __syncthreads();
-  const int warp_off = warp > 0 ? sh[warp - 1] : 0;
-  *total = sh[nwarps - 1];
-  __syncthreads();
-  return warp_off + incl - v;
-}
-
 // I_t = set bits of the bitmap (in shared memory) in ascending order, by one
 // CTA of kStateThreads threads, in two phases.
 //  Scan: thread t takes G consecutive groups of four words (a contiguous run
@@ -180,19 +149,32 @@ __host__ __device__ inline int state_smem_words(int nwords_pad) { return 3 * nwo
 // ---------------------------------------------------------------------------
 // Prefill initialisation (per request)
 // ---------------------------------------------------------------------------
-__global__ void init_reset_kernel(SeqDev s, Dims d) {
+// Entries the reset touches: the counts, the bitmaps and the slot table.
+__host__ __device__ inline int reset_extent(const Dims &d) {
   const int n = d.V > d.nwords_pad ? d.V : d.nwords_pad;
+  return n > d.W_max ? n : d.W_max;
+}
+
+// An empty stream: no entries, an empty window, and an empty slot table.
+__global__ void init_reset_kernel(SeqDev s, Dims d) {
+  const int n = reset_extent(d);
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     if (i < d.V) {
       s.counts[i] = 0u;
       if (d.K_pre > 0) s.first[i] = 0x7fffffff;
     }
-    if (i < d.nwords_pad) s.bitmap[i] = 0u;
+    if (i < d.nwords_pad) {
+      s.bitmap[i] = 0u;
+      s.held[i] = 0u;
+    }
+    if (i < d.W_max) s.slot_id[i] = -1;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     s.length[0] = 0;
     s.length[1] = 0;
     *s.count = 0;
+    s.slot_meta[0] = 0;
+    s.slot_meta[1] = 0;
   }
 }
 
@@ -801,7 +783,7 @@ bool cluster_fits(int n, int bytes) {
 
 cudaError_t launch_init(const SeqDev &s, const Dims &d, const int32_t *prompt, int L, const float *prefill,
                         uint32_t *err, cudaStream_t st) {
-  const int n = d.V > d.nwords_pad ? d.V : d.nwords_pad;
+  const int n = reset_extent(d);
   init_reset_kernel<<<(n + 255) / 256, 256, 0, st>>>(s, d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -61,7 +61,7 @@ constexpr int kStageB = kUN * kUK * 2;       // 8 KB
 constexpr int kStage = kStageA + kStageB;    // 24 KB (1024-byte multiple)
 constexpr int kRingBytes = kUStages * kStage;
 constexpr int kPartBytes = kUN * kUM * 4;    // one CTA's partial tile, [r][j] fp32
-constexpr int kMiscBytes = 1024;             // barriers, TMEM slot, ticket flag, row ids
+constexpr int kMiscBytes = 1280;             // barriers, TMEM slot, ticket flag, row ids, slot ids
 constexpr int kUSmem = kRingBytes + kMiscBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 64;
 
@@ -185,7 +185,10 @@ struct UmmaArgs {
   uint32_t *err;
 };
 
-template <int kUCluster>
+// kSlots: the rows come from the slot buffer instead (row j of a tile is slot
+// row0 + j, read in place and not stored back) and the top-k maps each slot to
+// the id it holds, skipping free slots (count_ptr is the high-water mark).
+template <int kUCluster, bool kSlots>
 __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2)
     umma_step_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmP,
                      UmmaArgs a) {
@@ -199,7 +202,8 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
   const uint32_t bar_acc = bar_empty + 8 * kUStages;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kRingBytes + 16 * kUStages + 8);
   int *s_flag = reinterpret_cast<int *>(gbase + kRingBytes + 16 * kUStages + 16);
-  int *s_rows = reinterpret_cast<int *>(gbase + kRingBytes + 256);  // 128 row ids
+  int *s_rows = reinterpret_cast<int *>(gbase + kRingBytes + 256);  // 128 source rows (ids, or slots)
+  int *s_ids = s_rows + kUM;                                         // 128 slot ids (kSlots)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = cluster_rank();
@@ -212,7 +216,7 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
     tma_prefetch(&tmP);
     for (int s = 0; s < kUStages; ++s) {
       mbar_init(bar_full + 8 * s, 1 + kGatherThreads);  // the TMA issuer and every gather thread
-      mbar_init(bar_empty + 8 * s, 2);                  // the MMA commit and the packed-store issuer
+      mbar_init(bar_empty + 8 * s, kSlots ? 1 : 2);     // the MMA commit (and the packed-store issuer)
     }
     mbar_init(bar_acc, 1);
     mbar_fence_init();
@@ -254,11 +258,20 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
     const int j = row0 + tid;
     if (j < m) {
       int id = iter == 0 ? id_first : a.idx[j];
-      if ((unsigned)id >= (unsigned)a.V) {  // I_t only holds valid ids
-        atomicOr(a.err, NS_FLAG_INTERNAL | (3u << 8));
-        id = 0;
+      if (kSlots) {
+        if (id < -1 || id >= a.V) {  // a slot holds a valid id or is free (-1)
+          atomicOr(a.err, NS_FLAG_INTERNAL | (3u << 8));
+          id = -1;
+        }
+        s_ids[tid] = id;
+        s_rows[tid] = j;
+      } else {
+        if ((unsigned)id >= (unsigned)a.V) {  // I_t only holds valid ids
+          atomicOr(a.err, NS_FLAG_INTERNAL | (3u << 8));
+          id = 0;
+        }
+        s_rows[tid] = id;
       }
-      s_rows[tid] = id;
     }
   }
   __syncthreads();
@@ -323,7 +336,7 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
     }
     if (nk > 0 && ok) umma_commit(bar_acc);
     else mbar_arrive(bar_acc);
-  } else if (warp == 2 && lane == 0) {
+  } else if (!kSlots && warp == 2 && lane == 0) {
     int released = 0;
     for (int kt = 0; kt < nk; ++kt) {
       const int g = iter * nk + kt, s = g % kUStages;
@@ -397,8 +410,9 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int j = lane + 32 * q;
-      hk[q] = row0 + j < m ? order_key(F[warp * kUM + j]) : 0u;
-      hi[q] = hk[q] != 0u ? (uint32_t)s_rows[j] : (uint32_t)kEmptyId;
+      const bool live = row0 + j < m && (!kSlots || s_ids[j] >= 0);
+      hk[q] = live ? order_key(F[warp * kUM + j]) : 0u;
+      hi[q] = hk[q] != 0u ? (uint32_t)(kSlots ? s_ids[j] : s_rows[j]) : (uint32_t)kEmptyId;
     }
     const size_t o = ((size_t)tile * kUN + r) * a.k;
     warp_topk4(hk, hi, a.k, a.cand_k + o, a.cand_i + o);
@@ -476,7 +490,7 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
   __syncwarp();
   cluster_sync();  // peers may still be reading this CTA's partial tile
   }  // tiles
-  if (warp == 2 && lane == 0) bulk_wait_all();  // the packed-buffer stores are complete before the CTA leaves
+  if (!kSlots && warp == 2 && lane == 0) bulk_wait_all();  // the packed-buffer stores are complete before the CTA leaves
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
@@ -539,19 +553,26 @@ int max_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, umma_step_kernel<CL>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, umma_step_kernel<CL, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return clusters;
 }
 
+template <int CL, bool SLOTS>
+cudaError_t allow_umma() {
+  cudaError_t e = cudaFuncSetAttribute(umma_step_kernel<CL, SLOTS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
+  if (e == cudaSuccess && CL > 8)
+    e = cudaFuncSetAttribute(umma_step_kernel<CL, SLOTS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
 cudaError_t prepare_umma_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(umma_step_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(umma_step_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(umma_step_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = allow_umma<8, false>();
+  if (e == cudaSuccess) e = allow_umma<16, false>();
+  if (e == cudaSuccess) e = allow_umma<8, true>();
+  if (e == cudaSuccess) e = allow_umma<16, true>();
   if (e != cudaSuccess) return e;
   if (!encoder()) return cudaErrorNotSupported;
   g_max16 = max_clusters<16>();
@@ -591,8 +612,12 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = L.programmatic ? 1 : 0;
-  if (CL == 16) return cudaLaunchKernelEx(&cfg, umma_step_kernel<16>, tmH, tmP, a);
-  return cudaLaunchKernelEx(&cfg, umma_step_kernel<8>, tmH, tmP, a);
+  if (L.slots) {
+    if (CL == 16) return cudaLaunchKernelEx(&cfg, umma_step_kernel<16, true>, tmH, tmP, a);
+    return cudaLaunchKernelEx(&cfg, umma_step_kernel<8, true>, tmH, tmP, a);
+  }
+  if (CL == 16) return cudaLaunchKernelEx(&cfg, umma_step_kernel<16, false>, tmH, tmP, a);
+  return cudaLaunchKernelEx(&cfg, umma_step_kernel<8, false>, tmH, tmP, a);
 }
 
 }  // namespace ns

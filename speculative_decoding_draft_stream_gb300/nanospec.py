@@ -33,7 +33,8 @@ EXPORTED = (
     "ns_status_string", "ns_create", "ns_destroy", "ns_device_bytes", "ns_stream_init", "ns_stream_append",
     "ns_build_active_vocab", "ns_gather_head_rows", "ns_sub_lm_head_logits_topk", "ns_step",
     "ns_dense_lm_head_topk", "ns_get_active", "ns_get_state", "ns_get_error", "ns_state_update",
-    "ns_gather_sub_lm_head_topk", "ns_trace_events", "ns_dense_lm_head_topk_noalloc",
+    "ns_gather_sub_lm_head_topk", "ns_trace_events", "ns_dense_lm_head_topk_noalloc", "ns_gather_new_head_rows",
+    "ns_slot_lm_head_logits_topk", "ns_step_slots", "ns_get_slots",
 )
 NOALLOC_MAX_LOGITS = 1 << 20
 
@@ -81,6 +82,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "ns_gather_sub_lm_head_topk": (I32, [P, I32, U16P, U16P, I32, I32, P, I32, P, P, P]),
         "ns_trace_events": (I32, [P, ctypes.POINTER(P), I32]),
         "ns_dense_lm_head_topk_noalloc": (I32, [U16P, I32, I32, U16P, I32, I32, P, I32, P, P, P]),
+        "ns_gather_new_head_rows": (I32, [P, I32, U16P, P, P]),
+        "ns_slot_lm_head_logits_topk": (I32, [P, I32, U16P, I32, I32, P, I32, P, P, P]),
+        "ns_step_slots": (I32, [P, I32, P, I32, P, I32, I32, U16P, U16P, I32, I32, P, I32, P, P, P]),
+        "ns_get_slots": (I32, [P, I32] + [ctypes.POINTER(P)] * 5),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -242,6 +247,51 @@ class Handle:
                                                     _ptr(ids, torch.int32, "ids"), _ptr(vals, torch.float32, "vals"),
                                                     _stream(stream)), "ns_gather_sub_lm_head_topk")
         return ids, vals
+
+    # -- the slot-stable buffer (incremental gather) ---------------------------
+    def gather_new_head_rows(self, seq: int, W_head: torch.Tensor, copy_stream=None,
+                             done: Optional[torch.cuda.Event] = None) -> None:
+        ev = done.cuda_event if done is not None else None
+        _check(self._lib.ns_gather_new_head_rows(self._h, seq, _ptr(W_head, _BF16, "W_head"), _stream(copy_stream),
+                                                 ev), "ns_gather_new_head_rows")
+
+    def slot_lm_head_logits_topk(self, seq: int, hidden: torch.Tensor, k: int,
+                                 logits: Optional[torch.Tensor] = None, ids: Optional[torch.Tensor] = None,
+                                 vals: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        n = hidden.shape[0]
+        ids, vals = self._outputs(n, k, ids, vals)
+        ld = logits.shape[1] if logits is not None else 0
+        _check(self._lib.ns_slot_lm_head_logits_topk(self._h, seq, _ptr(hidden, _BF16, "hidden"), n, k,
+                                                     _ptr(logits, torch.float32, "logits"), ld,
+                                                     _ptr(ids, torch.int32, "ids"), _ptr(vals, torch.float32, "vals"),
+                                                     _stream(stream)), "ns_slot_lm_head_logits_topk")
+        return ids, vals
+
+    def step_slots(self, seq: int, tree_ids: Optional[torch.Tensor], verify_logits: Optional[torch.Tensor],
+                   verify_row: int, W_head: torch.Tensor, hidden: torch.Tensor, k: int,
+                   logits: Optional[torch.Tensor] = None, ids: Optional[torch.Tensor] = None,
+                   vals: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        n_tree = 0 if tree_ids is None else tree_ids.numel()
+        n_v = 0 if verify_logits is None else (verify_logits.shape[0] if verify_logits.dim() == 2 else 1)
+        n = hidden.shape[0]
+        ids, vals = self._outputs(n, k, ids, vals)
+        ld = logits.shape[1] if logits is not None else 0
+        _check(self._lib.ns_step_slots(self._h, seq, _ptr(tree_ids, torch.int32, "tree_ids"), n_tree,
+                                       _ptr(verify_logits, torch.float32, "verify_logits"), n_v, verify_row,
+                                       _ptr(W_head, _BF16, "W_head"), _ptr(hidden, _BF16, "hidden"), n, k,
+                                       _ptr(logits, torch.float32, "logits"), ld, _ptr(ids, torch.int32, "ids"),
+                                       _ptr(vals, torch.float32, "vals"), _stream(stream)), "ns_step_slots")
+        return ids, vals
+
+    def get_slots(self, seq: int):
+        """Views (slot_id int32 [W_max], meta int32 [2] = (high-water mark, rows copied by the last update),
+        new_slots int32 [W_max], new_ids int32 [W_max], rows int16 [W_max, H])."""
+        p = [ctypes.c_void_p() for _ in range(5)]
+        _check(self._lib.ns_get_slots(self._h, seq, *[ctypes.byref(x) for x in p]), "ns_get_slots")
+        c = self.cfg
+        return (_view(p[0].value, (c.W_max,), "<i4", self.device), _view(p[1].value, (2,), "<i4", self.device),
+                _view(p[2].value, (c.W_max,), "<i4", self.device), _view(p[3].value, (c.W_max,), "<i4", self.device),
+                _view(p[4].value, (c.W_max, c.H), "<i2", self.device))
 
     def trace_events(self, events) -> None:
         """Record ns_step's kernel boundaries on four torch.cuda.Events (None: off)."""
