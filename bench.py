@@ -514,6 +514,63 @@ def run_ours(args):
 
         hid_bf = hid_d[0].view(torch.bfloat16)
         W_bf = W_d.view(torch.bfloat16)
+
+        # the PyTorch way on the same |I_t|: index_select of the rows (a
+        # packed copy), a cuBLAS GEMM and torch.topk (the ids stay indices
+        # into I_t; the remap would be one more gather)
+        idx_m = act[:m0].long()
+        sel = torch.empty((m0, H), dtype=torch.bfloat16, device=dev)
+        sub = torch.empty((n, m0), dtype=torch.bfloat16, device=dev)
+        us_torch = graph_us(lambda: (torch.index_select(W_bf, 0, idx_m, out=sel),
+                                     torch.matmul(hid_bf, sel.t(), out=sub), torch.topk(sub.float(), k, dim=1)))
+        extra["pinned_point"]["torch_index_select_matmul_topk_us"] = us_torch
+
+        # two-stream pipeline (MicroSpec §3.3): the gather of W_head[I_t, :] on a
+        # copy stream while a stand-in draft backbone runs on the compute
+        # stream, which waits for the gather only before the projection.
+        # Stand-ins: one Llama-3-8B-sized decoder layer's weights read once by
+        # the n tree tokens (HBM-bound, 4 x H^2 + 3 x H x 14336 bf16 weights),
+        # and four 2048^3 bf16 GEMMs (tensor-bound).
+        copy_s = torch.cuda.Stream()
+        n_layer = 4 * H + 3 * 14336
+        W_layer = torch.empty((n_layer, H), dtype=torch.bfloat16, device=dev).normal_(0.0, 0.02)
+        y_layer = torch.empty((n, n_layer), dtype=torch.bfloat16, device=dev)
+        xs = torch.empty((2048, 2048), dtype=torch.bfloat16, device=dev).normal_()
+        ys = torch.empty((2048, 2048), dtype=torch.bfloat16, device=dev)
+
+        def layer():
+            torch.matmul(hid_bf, W_layer.t(), out=y_layer)
+
+        def square():
+            for _ in range(4):
+                torch.matmul(xs, xs, out=ys)
+
+        def gather():
+            h.gather_head_rows(0, W_d, copy_stream=torch.cuda.current_stream())
+
+        def project():
+            h.sub_lm_head_logits_topk(0, hid_d[0], k, logits=logits, ids=ids, vals=vals)
+
+        def overlapped(backbone):
+            cur = torch.cuda.current_stream()
+            copy_s.wait_stream(cur)
+            h.gather_head_rows(0, W_d, copy_stream=copy_s)
+            backbone()
+            cur.wait_stream(copy_s)
+            project()
+
+        init()
+        h.build_active_vocab(0)
+        us_gather, us_project = graph_us(gather), graph_us(project)
+        ov = {"active": m0, "gather_us": us_gather, "project_us": us_project}
+        for name, bb in (("decoder_layer", layer), ("square_gemms", square)):
+            us_bb = graph_us(bb)
+            us_serial = graph_us(lambda: (bb(), gather(), project()))
+            us_ov = graph_us(lambda: overlapped(bb))
+            ov[name] = {"backbone_us": us_bb, "serial_us": us_serial, "overlapped_us": us_ov,
+                        "gather_hidden_frac": (us_serial - us_ov) / us_gather}
+        extra["copy_stream_overlap"] = ov
+        del W_layer, y_layer, xs, ys
         dense_out = torch.empty((n, V), dtype=torch.bfloat16, device=dev)
         dense_logits = torch.empty((n, V), dtype=torch.float32, device=dev)
         us_cublas = graph_us(lambda: torch.matmul(hid_bf, W_bf.t(), out=dense_out))

@@ -69,8 +69,6 @@ void layout(ns_handle *h, Carver &cv) {
     s.length = cv.take<long long>(2);
     s.packed = cv.take<uint16_t>((size_t)c.W_max * c.H);
     s.logits = cv.take<float>((size_t)ns::kProjBN * d.ld_scratch);
-    s.ppart = cv.take<float>((size_t)h->pgrid * ns::kProjBN * ns::kProjBM);
-    s.pticket = cv.take<int32_t>(h->pgrid);
     s.first = c.K_pre > 0 ? cv.take<int32_t>(c.V) : nullptr;
     s.cand = c.K_pre > 0 ? cv.take<int32_t>((size_t)c.max_prompt * c.K_pre) : nullptr;
     s.sinit = cv.take<int32_t>((size_t)c.max_prompt * (1 + c.K_pre));
@@ -230,6 +228,58 @@ static ns_status check_proj_args(ns_handle *h, const uint16_t *d_hidden, int32_t
   return NS_OK;
 }
 
+// Trace events are recorded as external event nodes when the stream is being
+// captured into a CUDA graph (so a captured step still times its kernels) and
+// as plain records otherwise (the external flag is only valid in capture).
+static cudaError_t trace_record(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess) return e;
+  if (cap == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  return cudaEventRecord(ev, st);
+}
+
+// Where the fused tcgen05 kernel reads the rows of the sub-head from.
+enum class Rows {
+  kGather,  // W_head through I_t, storing them to the packed buffer on the way
+  kPacked,  // the packed buffer, row j = I_t[j] (after a separate gather)
+  kSlots,   // the slot buffer, row s = slot_id[s] (-1: free, not ranked)
+};
+
+// Projection + top-k (one tcgen05 kernel).  `mid` (nullable) is recorded
+// after it.  With `programmatic` the kernel may begin while the preceding
+// kernel finishes.
+static cudaError_t enqueue_gather_project(ns_handle *h, int32_t seq, const uint16_t *d_W_head,
+                                          const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
+                                          int32_t ld_logits, int32_t *d_ids, float *d_vals, cudaStream_t cs,
+                                          cudaEvent_t mid, bool programmatic, Rows rows = Rows::kGather) {
+  const ns::SeqDev &s = h->seqs[seq];
+  ns::UmmaLaunch L{};
+  L.W = rows == Rows::kGather ? d_W_head : rows == Rows::kPacked ? s.packed : s.slot_rows;
+  L.V = h->cfg.V;
+  L.H = h->cfg.H;
+  L.hid = d_hidden;
+  L.n = n;
+  L.packed = rows == Rows::kSlots ? s.slot_rows : s.packed;
+  L.W_max = h->cfg.W_max;
+  L.idx = rows == Rows::kSlots ? s.slot_id : s.active;
+  L.count_ptr = rows == Rows::kSlots ? s.slot_meta : s.count;
+  L.in_place = rows != Rows::kGather;
+  L.k = k;
+  L.logits = d_logits ? d_logits : s.logits;
+  L.ld = d_logits ? ld_logits : h->dims.ld_scratch;
+  L.cand_k = s.cand_k;
+  L.cand_i = s.cand_i;
+  L.slice_ticket = s.slice_ticket;
+  L.out_ids = d_ids;
+  L.out_vals = d_vals;
+  L.err = h->err;
+  L.programmatic = programmatic;
+  cudaError_t e = ns::launch_umma_step(L, cs);
+  if (e == cudaSuccess && mid) e = trace_record(mid, cs);
+  return e;
+}
+
 ns_status ns_sub_lm_head_logits_topk(ns_handle *h, int32_t seq, const uint16_t *d_hidden, int32_t n, int32_t k,
                                      float *d_logits, int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
                                      ns_stream stream) {
@@ -237,21 +287,9 @@ ns_status ns_sub_lm_head_logits_topk(ns_handle *h, int32_t seq, const uint16_t *
   ns_status st = check_proj_args(h, d_hidden, n, k, d_logits, ld_logits, h->cfg.W_max, d_topk_ids, d_topk_vals);
   if (st != NS_OK) return st;
   if (!h->inited[seq]) return NS_ERR_STATE;
-  const ns::SeqDev &s = h->seqs[seq];
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  ns::ProjArgs a{};
-  a.rows = s.packed;
-  a.count_ptr = s.count;
-  a.hid = d_hidden;
-  a.n = n;
-  a.H = h->cfg.H;
-  a.logits = d_logits ? d_logits : s.logits;
-  a.ld = d_logits ? ld_logits : h->dims.ld_scratch;
-  a.part = s.ppart;
-  a.tickets = s.pticket;
-  cudaError_t e = ns::launch_project(ns::kFromPacked, a, h->pgrid, cs);
-  if (e == cudaSuccess) e = ns::launch_topk(a.logits, a.ld, s.count, 0, s.active, n, k, d_topk_ids, d_topk_vals, cs);
-  return cuda_status(e);
+  return cuda_status(enqueue_gather_project(h, seq, nullptr, d_hidden, n, k, d_logits, ld_logits, d_topk_ids,
+                                            d_topk_vals, static_cast<cudaStream_t>(stream), nullptr, false,
+                                            Rows::kPacked));
 }
 
 ns_status ns_state_update(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
@@ -271,51 +309,6 @@ static ns_status check_gather_project_args(ns_handle *h, int32_t seq, const uint
   if (st != NS_OK) return st;
   if (!h->inited[seq]) return NS_ERR_STATE;
   return NS_OK;
-}
-
-// Trace events are recorded as external event nodes when the stream is being
-// captured into a CUDA graph (so a captured step still times its kernels) and
-// as plain records otherwise (the external flag is only valid in capture).
-static cudaError_t trace_record(cudaEvent_t ev, cudaStream_t st) {
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  cudaError_t e = cudaStreamIsCapturing(st, &cap);
-  if (e != cudaSuccess) return e;
-  if (cap == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
-  return cudaEventRecord(ev, st);
-}
-
-// Fused gather + projection + top-k (one tcgen05 kernel).  `mid` (nullable)
-// is recorded after it.  With `programmatic` the kernel may begin while the
-// preceding state update finishes.
-static cudaError_t enqueue_gather_project(ns_handle *h, int32_t seq, const uint16_t *d_W_head,
-                                          const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
-                                          int32_t ld_logits, int32_t *d_ids, float *d_vals, cudaStream_t cs,
-                                          cudaEvent_t mid, bool programmatic, bool slots = false) {
-  const ns::SeqDev &s = h->seqs[seq];
-  ns::UmmaLaunch L{};
-  L.W = slots ? s.slot_rows : d_W_head;
-  L.V = h->cfg.V;
-  L.H = h->cfg.H;
-  L.hid = d_hidden;
-  L.n = n;
-  L.packed = slots ? s.slot_rows : s.packed;
-  L.W_max = h->cfg.W_max;
-  L.idx = slots ? s.slot_id : s.active;
-  L.count_ptr = slots ? s.slot_meta : s.count;
-  L.slots = slots;
-  L.k = k;
-  L.logits = d_logits ? d_logits : s.logits;
-  L.ld = d_logits ? ld_logits : h->dims.ld_scratch;
-  L.cand_k = s.cand_k;
-  L.cand_i = s.cand_i;
-  L.slice_ticket = s.slice_ticket;
-  L.out_ids = d_ids;
-  L.out_vals = d_vals;
-  L.err = h->err;
-  L.programmatic = programmatic;
-  cudaError_t e = ns::launch_umma_step(L, cs);
-  if (e == cudaSuccess && mid) e = trace_record(mid, cs);
-  return e;
 }
 
 ns_status ns_gather_sub_lm_head_topk(ns_handle *h, int32_t seq, const uint16_t *d_W_head, const uint16_t *d_hidden,
@@ -367,7 +360,8 @@ ns_status ns_slot_lm_head_logits_topk(ns_handle *h, int32_t seq, const uint16_t 
   if (st != NS_OK) return st;
   if (!h->inited[seq]) return NS_ERR_STATE;
   return cuda_status(enqueue_gather_project(h, seq, nullptr, d_hidden, n, k, d_logits, ld_logits, d_topk_ids,
-                                            d_topk_vals, static_cast<cudaStream_t>(stream), nullptr, false, true));
+                                            d_topk_vals, static_cast<cudaStream_t>(stream), nullptr, false,
+                                            Rows::kSlots));
 }
 
 ns_status ns_step_slots(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
@@ -384,7 +378,7 @@ ns_status ns_step_slots(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, in
   if (e == cudaSuccess) e = ns::launch_slot_update(h->seqs[seq], h->dims, d_W_head, h->sgrid, h->err, cs);
   if (e == cudaSuccess)
     e = enqueue_gather_project(h, seq, nullptr, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals, cs,
-                               nullptr, true, true);
+                               nullptr, true, Rows::kSlots);
   return cuda_status(e);
 }
 
@@ -420,7 +414,7 @@ ns_status ns_dense_lm_head_topk(ns_handle *h, const uint16_t *d_W_head, int32_t 
   a.ld = d_logits ? ld_logits : h->dense_ld;
   a.part = h->dense_part;
   a.tickets = h->dense_tickets;
-  cudaError_t e = ns::launch_project(ns::kDenseRows, a, h->pgrid, cs);
+  cudaError_t e = ns::launch_project(a, h->pgrid, cs);
   if (e == cudaSuccess) e = ns::launch_topk(a.logits, a.ld, nullptr, rows, nullptr, n, k, d_topk_ids, d_topk_vals, cs);
   return cuda_status(e);
 }

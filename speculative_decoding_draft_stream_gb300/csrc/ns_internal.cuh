@@ -33,8 +33,6 @@ struct SeqDev {
   long long *length;  // [2] |S|, then |S| mod W_max (the ring slot of the next entry)
   uint16_t *packed;   // [W_max x H] bf16 rows W_head[I_t[j], :]
   float *logits;      // [kProjBN x ld_scratch] fp32 logits when the caller passes none
-  float *ppart;       // [proj_grid x kProjBN x kProjBM] split-K partial tiles
-  int32_t *pticket;   // [proj_grid] per-tile arrival counters
   int32_t *first;     // [V] first flat index of an id in the prefill union (init only)
   int32_t *cand;      // [max_prompt x K_pre] prefill Top-K ids (init only)
   int32_t *sinit;     // [max_prompt x (1 + K_pre)] S_init entries (init only)
@@ -331,15 +329,10 @@ cudaError_t prepare_slot_kernels(const Dims &d);
 cudaError_t launch_slot_update(const SeqDev &s, const Dims &d, const uint16_t *W, int copy_grid, uint32_t *err,
                                cudaStream_t st);
 
-// Projection source modes.
-enum ProjMode { kFromPacked = 0, kGatherRows = 1, kDenseRows = 2 };
-
+// Dense head (ns_project.cu): rows [0, rows_host) of W_head.
 struct ProjArgs {
-  const uint16_t *rows;      // packed buffer (kFromPacked) or W_head
-  const int32_t *idx;        // I_t (kGatherRows)
-  const int32_t *count_ptr;  // device row count (kFromPacked / kGatherRows)
-  int32_t rows_host;         // row count (kDenseRows)
-  uint16_t *packed_out;      // packed buffer to fill (kGatherRows)
+  const uint16_t *rows;      // W_head
+  int32_t rows_host;         // row count
   const uint16_t *hid;       // [n x H]
   int32_t n, H;
   float *logits;             // [n x ld]
@@ -348,7 +341,7 @@ struct ProjArgs {
   int32_t *tickets;          // per-tile arrival counters
 };
 
-cudaError_t launch_project(ProjMode mode, const ProjArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_project(const ProjArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_topk(const float *logits, int ld, const int32_t *count_ptr, int rows_host,
                         const int32_t *idmap, int n, int k, int32_t *ids, float *vals, cudaStream_t st);
 
@@ -375,7 +368,7 @@ struct UmmaLaunch {
   float *out_vals;
   uint32_t *err;
   bool programmatic;         // may start while the preceding kernel finishes
-  bool slots;                // rows from the slot buffer (W = slot rows, idx = slot ids, count = high-water mark)
+  bool in_place;             // rows already in a contiguous buffer W (row j = id idx[j], -1 = skip), not stored
 };
 int umma_tiles(int W_max);
 int umma_cluster();

@@ -105,7 +105,7 @@ extern "C" ns_status ns_dense_lm_head_topk_noalloc(const uint16_t *d_W_head, int
   a.ld = d_logits ? ld_logits : rows;
   a.part = base + kPartOff;
   a.tickets = tickets;
-  cudaError_t e = ns::launch_project(ns::kDenseRows, a, s->grid, cs);
+  cudaError_t e = ns::launch_project(a, s->grid, cs);
   if (e == cudaSuccess) e = ns::launch_topk(a.logits, a.ld, nullptr, rows, nullptr, n, k, d_topk_ids, d_topk_vals, cs);
   return e == cudaSuccess ? NS_OK : NS_ERR_CUDA;
 }

@@ -1,21 +1,17 @@
-// Sub-head projection logits[r, j] = sum_h hidden[r, h] * rows[j, h]
-// (MicroSpec §3.1 Eq. 1 restricted to W_head[I_t, :]) and the per-row top-k
-// with the remap of column j to the global id I_t[j].
+// Dense head on a row range of W_head: logits[r, j] = sum_h hidden[r, h] *
+// W_head[j, h] for j < rows (MicroSpec §3.1 Eq. 1 over the whole vocabulary,
+// or over a static first-rows sub-head) and the per-row top-k with ids = row
+// numbers.  These are the comparators of the dynamic sub-head, whose own
+// projection runs in the fused tcgen05 kernel.
 //
 // Projection kernel.  A tile is 64 W_head rows x 64 hidden rows; the K loop
 // streams 64-wide k slices of both operands through a 4-stage cp.async
 // pipeline into 128-byte-swizzled shared memory, and four warps each
 // multiply 16 rows against all 64 hidden rows with bf16 tensor-core MMAs
-// (fp32 accumulate).  The number of row tiles depends on |I_t|, which only
-// the device knows, so the grid is fixed (two CTAs per SM) and each CTA
-// derives its work from the device count: when there are fewer tiles than
-// CTAs, K is split S ways, partial tiles go to scratch, and the last CTA of a
-// tile to arrive adds them in split order (deterministic).
-//
-// In the gather mode the row operand is read straight from W_head through
-// I_t (MicroSpec §3.3: gather into the packed buffer, then a dense product):
-// every 16-byte chunk that lands in shared memory is also written to the
-// packed buffer, so W_head[I_t, :] is read from HBM once per step.
+// (mma.sync, fp32 accumulate).  The grid is fixed (two CTAs per SM); when
+// there are fewer tiles than CTAs, K is split S ways, partial tiles go to
+// scratch, and the last CTA of a tile to arrive adds them in split order
+// (deterministic).
 #include "ns_internal.cuh"
 
 namespace ns {
@@ -57,12 +53,11 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 // Byte offset of 16-byte chunk c of row r in a [rows x 128 B] swizzled stage.
 __device__ __forceinline__ int swz(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 
-template <int MODE>
 __global__ void __launch_bounds__(kProjThreads) project_kernel(ProjArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m = (MODE == kDenseRows) ? a.rows_host : *a.count_ptr;
+  const int m = a.rows_host;
   const int T = (m + kProjBM - 1) / kProjBM;
   if (T == 0) return;
   const int KC = a.H / kProjBK;
@@ -89,9 +84,7 @@ __global__ void __launch_bounds__(kProjThreads) project_kernel(ProjArgs a) {
       const int r = (tid >> 3) + 16 * q;
       const int j = row0 + r;
       const bool av = j < m;
-      int id = av ? j : 0;
-      if (MODE == kGatherRows && av) id = a.idx[j];
-      asrc[q] = a.rows + (size_t)id * a.H + c * 8;
+      asrc[q] = a.rows + (size_t)(av ? j : 0) * a.H + c * 8;
       abytes[q] = av ? 16u : 0u;
       const bool bv = r < a.n;
       bsrc[q] = a.hid + (size_t)(bv ? r : 0) * a.H + c * 8;
@@ -126,17 +119,6 @@ __global__ void __launch_bounds__(kProjThreads) project_kernel(ProjArgs a) {
       const int slot = kt % kProjStages;
       const uint8_t *As = smem + slot * kStageBytes;
       const uint8_t *Bs = As + kStageBytesA;
-      if (MODE == kGatherRows) {
-        const int koff = (kc0 + kt) * kProjBK;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (abytes[q]) {
-            const int r = (tid >> 3) + 16 * q;
-            const uint4 v = *reinterpret_cast<const uint4 *>(As + swz(r, c));
-            *reinterpret_cast<uint4 *>(a.packed_out + (size_t)(row0 + r) * a.H + koff + c * 8) = v;
-          }
-        }
-      }
 #pragma unroll
       for (int kk = 0; kk < kProjBK / 16; ++kk) {
         uint32_t af[4];
@@ -220,7 +202,7 @@ __global__ void __launch_bounds__(kProjThreads) project_kernel(ProjArgs a) {
 }
 
 // Per-row top-k over logits[r, 0:m): one CTA per hidden row.  Column j stands
-// for global id idmap[j] (I_t, ascending) or j itself.
+// for global id idmap[j] when idmap is given, else for j itself.
 template <int KMAX>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *logits, int ld, const int32_t *count_ptr,
                                                             int rows_host, const int32_t *idmap, int k, int32_t *ids,
@@ -249,22 +231,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float *logits,
 size_t project_smem_bytes() { return (size_t)kProjStages * kStageBytes; }
 
 cudaError_t prepare_project_kernels() {
-  const int bytes = (int)project_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(project_kernel<kFromPacked>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(project_kernel<kGatherRows>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(project_kernel<kDenseRows>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  return e;
+  return cudaFuncSetAttribute(project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)project_smem_bytes());
 }
 
-cudaError_t launch_project(ProjMode mode, const ProjArgs &a, int grid, cudaStream_t st) {
-  const size_t smem = project_smem_bytes();
-  switch (mode) {
-    case kFromPacked: project_kernel<kFromPacked><<<grid, kProjThreads, smem, st>>>(a); break;
-    case kGatherRows: project_kernel<kGatherRows><<<grid, kProjThreads, smem, st>>>(a); break;
-    default: project_kernel<kDenseRows><<<grid, kProjThreads, smem, st>>>(a); break;
-  }
+cudaError_t launch_project(const ProjArgs &a, int grid, cudaStream_t st) {
+  project_kernel<<<grid, kProjThreads, project_smem_bytes(), st>>>(a);
   return cudaGetLastError();
 }
 

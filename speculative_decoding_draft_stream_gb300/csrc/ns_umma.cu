@@ -185,10 +185,12 @@ struct UmmaArgs {
   uint32_t *err;
 };
 
-// kSlots: the rows come from the slot buffer instead (row j of a tile is slot
-// row0 + j, read in place and not stored back) and the top-k maps each slot to
-// the id it holds, skipping free slots (count_ptr is the high-water mark).
-template <int kUCluster, bool kSlots>
+// kInPlace: the rows come from a contiguous buffer that already holds them
+// (the packed buffer after a separate gather, or the slot buffer): row j of a
+// tile is buffer row row0 + j, read in place and not stored back, and the
+// top-k maps row j to the id idx[j], skipping rows whose id is -1 (free slots;
+// count_ptr is then the slot table's high-water mark).
+template <int kUCluster, bool kInPlace>
 __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2)
     umma_step_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmP,
                      UmmaArgs a) {
@@ -203,7 +205,7 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kRingBytes + 16 * kUStages + 8);
   int *s_flag = reinterpret_cast<int *>(gbase + kRingBytes + 16 * kUStages + 16);
   int *s_rows = reinterpret_cast<int *>(gbase + kRingBytes + 256);  // 128 source rows (ids, or slots)
-  int *s_ids = s_rows + kUM;                                         // 128 slot ids (kSlots)
+  int *s_ids = s_rows + kUM;                                         // 128 ids of the rows (kInPlace)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = cluster_rank();
@@ -216,7 +218,7 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
     tma_prefetch(&tmP);
     for (int s = 0; s < kUStages; ++s) {
       mbar_init(bar_full + 8 * s, 1 + kGatherThreads);  // the TMA issuer and every gather thread
-      mbar_init(bar_empty + 8 * s, kSlots ? 1 : 2);     // the MMA commit (and the packed-store issuer)
+      mbar_init(bar_empty + 8 * s, kInPlace ? 1 : 2);     // the MMA commit (and the packed-store issuer)
     }
     mbar_init(bar_acc, 1);
     mbar_fence_init();
@@ -258,8 +260,8 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
     const int j = row0 + tid;
     if (j < m) {
       int id = iter == 0 ? id_first : a.idx[j];
-      if (kSlots) {
-        if (id < -1 || id >= a.V) {  // a slot holds a valid id or is free (-1)
+      if (kInPlace) {
+        if (id < -1 || id >= a.V) {  // a row holds a valid id or is a free slot (-1)
           atomicOr(a.err, NS_FLAG_INTERNAL | (3u << 8));
           id = -1;
         }
@@ -336,7 +338,7 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
     }
     if (nk > 0 && ok) umma_commit(bar_acc);
     else mbar_arrive(bar_acc);
-  } else if (!kSlots && warp == 2 && lane == 0) {
+  } else if (!kInPlace && warp == 2 && lane == 0) {
     int released = 0;
     for (int kt = 0; kt < nk; ++kt) {
       const int g = iter * nk + kt, s = g % kUStages;
@@ -410,9 +412,9 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int j = lane + 32 * q;
-      const bool live = row0 + j < m && (!kSlots || s_ids[j] >= 0);
+      const bool live = row0 + j < m && (!kInPlace || s_ids[j] >= 0);
       hk[q] = live ? order_key(F[warp * kUM + j]) : 0u;
-      hi[q] = hk[q] != 0u ? (uint32_t)(kSlots ? s_ids[j] : s_rows[j]) : (uint32_t)kEmptyId;
+      hi[q] = hk[q] != 0u ? (uint32_t)(kInPlace ? s_ids[j] : s_rows[j]) : (uint32_t)kEmptyId;
     }
     const size_t o = ((size_t)tile * kUN + r) * a.k;
     warp_topk4(hk, hi, a.k, a.cand_k + o, a.cand_i + o);
@@ -490,7 +492,7 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
   __syncwarp();
   cluster_sync();  // peers may still be reading this CTA's partial tile
   }  // tiles
-  if (!kSlots && warp == 2 && lane == 0) bulk_wait_all();  // the packed-buffer stores are complete before the CTA leaves
+  if (!kInPlace && warp == 2 && lane == 0) bulk_wait_all();  // the packed-buffer stores are complete before the CTA leaves
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
@@ -612,7 +614,7 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = L.programmatic ? 1 : 0;
-  if (L.slots) {
+  if (L.in_place) {
     if (CL == 16) return cudaLaunchKernelEx(&cfg, umma_step_kernel<16, true>, tmH, tmP, a);
     return cudaLaunchKernelEx(&cfg, umma_step_kernel<8, true>, tmH, tmP, a);
   }
