@@ -52,6 +52,9 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-extra", action="store_true", help="skip the dense-head and pinned-point extras")
+    p.add_argument("--sweep", action="store_true",
+                   help="also time the Qwen-2.5-7B-shaped workload and the Qwen3-8B W_max sweep (with its dense "
+                        "heads) into extra.workloads")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
     p.add_argument("--decode-steps", type=int, default=0,
                    help="generate inputs for only this many decode steps (0: the workload's count); "
@@ -227,6 +230,155 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # our CUDA path
 # ---------------------------------------------------------------------------
+def graph_time_us(fn, flush, reps=32):
+    """Device time of fn in us: (graph of reps x [flush + fn]) - (graph of reps x [flush])."""
+    import torch
+
+    def capture(with_op):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                flush.zero_()
+                if with_op:
+                    fn()
+        return g
+
+    fn()
+    torch.cuda.synchronize()
+    g_op, g_fl = capture(True), capture(False)
+    out = []
+    for g in (g_op, g_fl, g_op, g_fl):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        out.append(a.elapsed_time(b))
+    return 1e3 * min(out[0] - out[1], out[2] - out[3]) / reps
+
+
+def decode_inputs(cfg, dev, seq=0):
+    """One sequence's inputs of a workload, on the device: W_head, prompt,
+    prefill logits, trees, verify rows and hiddens of every decode step."""
+    import torch
+    from synth import Workload
+
+    wl = Workload(cfg)
+    T = cfg.steps
+    return {"W": torch.from_numpy(wl.w_head().view(np.int16)).to(dev),
+            "prompt": torch.from_numpy(wl.prompt(seq)).to(dev),
+            "Z": torch.from_numpy(wl.prefill_logits(seq)).to(dev),
+            "trees": torch.from_numpy(wl.trees(seq)).to(dev),
+            "verify": torch.from_numpy(np.stack([wl.verify_logits(seq, t) for t in range(T)])).to(dev),
+            "vrows": [wl.verify_row(seq, t) for t in range(T)],
+            "hid": torch.from_numpy(np.stack([wl.hiddens(seq, t) for t in range(T)]).view(np.int16)).to(dev)}
+
+
+def time_decode(ns, cfg, dev, flush, warmup, inp):
+    """Per-step time of ns_step over every decode step of one workload (graph of
+    steps minus graph of flushes, median of three replays from the prefill
+    state) and the |I_t| of each step.  `inp` is decode_inputs(cfg, ...)."""
+    import torch
+
+    n, H, V, k, T = cfg.n_tree, cfg.H, cfg.V, cfg.k, cfg.steps
+    W_d, prompt_d, Z_d, trees_d = inp["W"], inp["prompt"], inp["Z"], inp["trees"]
+    verify_d, vrows, hid_d = inp["verify"], inp["vrows"], inp["hid"]
+    logits = torch.empty((n, cfg.W_max), dtype=torch.float32, device=dev)
+    ids = torch.empty((n, k), dtype=torch.int32, device=dev)
+    vals = torch.empty((n, k), dtype=torch.float32, device=dev)
+    h = ns.Handle(V, H, cfg.W_max, cfg.K_pre, cfg.K_ver, max_tree=n, max_k=k, max_prompt=prompt_d.numel())
+    try:
+        def init():
+            h.stream_init(0, prompt_d, Z_d)
+            h.build_active_vocab(0)
+
+        def step(t):
+            h.step(0, trees_d[t], verify_d[t], vrows[t], W_d, hid_d[t], k, logits=logits, ids=ids, vals=vals)
+
+        init()
+        for t in range(min(warmup, T)):
+            step(t)
+        torch.cuda.synchronize()
+        graphs = []
+        for with_steps in (True, False):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for t in range(T):
+                    flush.zero_()
+                    if with_steps:
+                        step(t)
+            graphs.append(g)
+        diffs = []
+        for _ in range(3):
+            ms = []
+            for g in graphs:
+                init()
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                torch.cuda.synchronize()
+                ms.append(a.elapsed_time(b))
+            diffs.append(ms[0] - ms[1])
+        del graphs
+        init()
+        _, cnt, _, _ = h.get_active(0)
+        counts = torch.zeros(T, dtype=torch.int32, device=dev)
+        for t in range(T):
+            step(t)
+            counts[t:t + 1].copy_(cnt)
+        m = counts.cpu().numpy()
+        if h.get_error() != 0:
+            raise RuntimeError(f"device error flags set during the {cfg.name} steps")
+        us = 1e3 * sorted(diffs)[1] / T
+        pb = float(np.mean([proj_bytes(int(x), n, H) for x in m]))
+        sb = float(np.mean([step_bytes(int(x), n, H, V) for x in m]))
+        return {"us_per_step": us, "steps_per_s": 1e6 / us, "steps": T, "mean_active": float(m.mean()),
+                "min_active": int(m.min()), "max_active": int(m.max()), "step_bytes_mean": sb,
+                "step_hbm_frac": sb / (us * 1e-6) / 1e9 / load_peaks()[0], "proj_bytes_mean": pb}
+    finally:
+        h.close()
+
+
+def run_sweep(ns, dev, flush, warmup):
+    """The other draft-head shapes: Qwen-2.5-7B (H = 3584) and the Qwen3-8B
+    W_max sweep, each point with its decode steps; the Qwen3 head also with
+    the full-vocabulary dense head (cuBLAS and ours) and the static first-32768
+    sub-head on the same hiddens."""
+    import torch
+    from synth import get_config
+
+    out = {}
+    q25 = get_config("qwen25_7b_v152064_h3584")
+    out[q25.name] = time_decode(ns, q25, dev, flush, warmup, decode_inputs(q25, dev))
+    torch.cuda.empty_cache()
+    q3 = get_config("qwen3_8b_v151936_h4096")
+    inp = decode_inputs(q3, dev)  # the inputs do not depend on W_max
+    pts = {}
+    for W_max in q3.W_max_sweep:
+        pts[str(W_max)] = time_decode(ns, q3.with_(W_max=W_max), dev, flush, warmup, inp)
+    W_d, hid = inp["W"], inp["hid"][0]
+    n, k, V = q3.n_tree, q3.k, q3.V
+    h = ns.Handle(V, q3.H, q3.W_max, q3.K_pre, q3.K_ver, max_tree=n, max_k=k, max_prompt=16)
+    try:
+        ids = torch.empty((n, k), dtype=torch.int32, device=dev)
+        vals = torch.empty((n, k), dtype=torch.float32, device=dev)
+        dl = torch.empty((n, V), dtype=torch.float32, device=dev)
+        dout = torch.empty((n, V), dtype=torch.bfloat16, device=dev)
+        hb, Wb = hid.view(torch.bfloat16), W_d.view(torch.bfloat16)
+        dense = {"cublas_matmul_us": graph_time_us(lambda: torch.matmul(hb, Wb.t(), out=dout), flush),
+                 "ours_dense_topk_us": graph_time_us(lambda: h.dense_lm_head_topk(W_d, V, hid, k, logits=dl,
+                                                                                  ids=ids, vals=vals), flush),
+                 "ours_static32768_topk_us": graph_time_us(lambda: h.dense_lm_head_topk(W_d, 32768, hid, k,
+                                                                                        logits=dl, ids=ids,
+                                                                                        vals=vals), flush)}
+    finally:
+        h.close()
+    out[q3.name] = {"W_max_sweep": pts, "dense_head": dense}
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -430,27 +582,7 @@ def run_ours(args):
     extra = {}
     if not args.no_extra:
         def graph_us(fn, reps=32):
-            def capture(with_op):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    for _ in range(reps):
-                        flush.zero_()
-                        if with_op:
-                            fn()
-                return g
-
-            fn()
-            torch.cuda.synchronize()
-            g_op, g_fl = capture(True), capture(False)
-            out = []
-            for g in (g_op, g_fl, g_op, g_fl):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                g.replay()
-                b.record()
-                torch.cuda.synchronize()
-                out.append(a.elapsed_time(b))
-            return 1e3 * min(out[0] - out[1], out[2] - out[3]) / reps
+            return graph_time_us(fn, flush, reps)
 
         # the slot-stable buffer: K steps of ns_step_slots (state update, slot
         # update + copy of the newly placed rows, projection over the slots),
@@ -582,6 +714,8 @@ def run_ours(args):
                                "ours_static32768_topk_us": us_static,
                                "speedup_step_vs_cublas_dense": us_cublas / (1e3 * total_ms / K),
                                "speedup_pinned_point_vs_cublas_dense": us_cublas / us0}
+    if args.sweep:
+        extra["workloads"] = run_sweep(ns, dev, flush, args.warmup)
     clock = clocks.stop()
 
     # ---- the CPU oracle on a bounded sample (rank 0, one GPU) ----------------
