@@ -376,7 +376,97 @@ def run_sweep(ns, dev, flush, warmup):
     finally:
         h.close()
     out[q3.name] = {"W_max_sweep": pts, "dense_head": dense}
+    del inp, W_d, hid
+    torch.cuda.empty_cache()
+    b16 = get_config("batched16_v128256_h4096")
+    out[b16.name] = time_batched(ns, b16, dev, flush, warmup)
     return out
+
+
+def time_batched(ns, cfg, dev, flush, warmup):
+    """The batched-serving workload: every decode step of all sequences by
+    ns_step_batch (two launches), against the same steps issued as one ns_step
+    per sequence; each timed from the prefill state (graph of steps minus
+    graph of flushes, median of three replays)."""
+    import torch
+    from synth import Workload
+
+    wl = Workload(cfg)
+    B, n, H, V, k, T = cfg.batch, cfg.n_tree, cfg.H, cfg.V, cfg.k, cfg.steps
+    W_d = torch.from_numpy(wl.w_head().view(np.int16)).to(dev)
+    prompts = [torch.from_numpy(wl.prompt(b)).to(dev) for b in range(B)]
+    Zs = [torch.from_numpy(wl.prefill_logits(b)).to(dev) for b in range(B)]
+    trees_d = torch.from_numpy(np.ascontiguousarray(np.stack([wl.trees(b)[:T] for b in range(B)], axis=1))).to(dev)
+    verify_d = torch.from_numpy(np.stack([np.stack([wl.verify_logits(b, t) for b in range(B)])
+                                          for t in range(T)])).to(dev)  # [T, B, n_v, V]
+    vrows = [[wl.verify_row(b, t) for b in range(B)] for t in range(T)]
+    hid_d = torch.from_numpy(np.stack([np.stack([wl.hiddens(b, t) for b in range(B)])
+                                       for t in range(T)]).view(np.int16)).to(dev)  # [T, B, n, H]
+    logits = torch.empty((B, n, cfg.W_max), dtype=torch.float32, device=dev)
+    ids = torch.empty((B, n, k), dtype=torch.int32, device=dev)
+    vals = torch.empty((B, n, k), dtype=torch.float32, device=dev)
+    h = ns.Handle(V, H, cfg.W_max, cfg.K_pre, cfg.K_ver, max_tree=n, max_k=k, batch=B,
+                  max_prompt=max(p.numel() for p in prompts))
+    try:
+        def init():
+            for b in range(B):
+                h.stream_init(b, prompts[b], Zs[b])
+                h.build_active_vocab(b)
+
+        def batched(t):
+            h.step_batch(trees_d[t], verify_d[t], vrows[t], W_d, hid_d[t], k, logits=logits, ids=ids, vals=vals)
+
+        def one_by_one(t):
+            for b in range(B):
+                h.step(b, trees_d[t, b], verify_d[t, b], vrows[t][b], W_d, hid_d[t, b], k, logits=logits[b],
+                       ids=ids[b], vals=vals[b])
+
+        def per_step_us(fn):
+            init()
+            for t in range(min(warmup, T)):
+                fn(t)
+            torch.cuda.synchronize()
+            graphs = []
+            for with_steps in (True, False):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for t in range(T):
+                        flush.zero_()
+                        if with_steps:
+                            fn(t)
+                graphs.append(g)
+            diffs = []
+            for _ in range(3):
+                ms = []
+                for g in graphs:
+                    init()
+                    torch.cuda.synchronize()
+                    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    g.replay()
+                    e.record()
+                    torch.cuda.synchronize()
+                    ms.append(a.elapsed_time(e))
+                diffs.append(ms[0] - ms[1])
+            return 1e3 * sorted(diffs)[1] / T
+
+        us_b = per_step_us(batched)
+        us_s = per_step_us(one_by_one)
+        init()
+        _, cnt, _, _ = h.get_active(0)
+        act = torch.zeros((T, B), dtype=torch.int32, device=dev)
+        for t in range(T):
+            batched(t)
+            for b in range(B):
+                act[t, b:b + 1].copy_(h.get_active(b)[1])
+        act = act.cpu().numpy()
+        if h.get_error() != 0:
+            raise RuntimeError("device error flags set during the batched steps")
+        return {"sequences": B, "steps": T, "batched_step_us": us_b, "sequence_steps_per_s": B * 1e6 / us_b,
+                "one_call_per_sequence_step_us": us_s, "speedup_batched": us_s / us_b,
+                "mean_active": float(act.mean())}
+    finally:
+        h.close()
 
 
 def run_ours(args):

@@ -189,6 +189,27 @@ NS_API ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, i
                   ns_stream stream);
 
 /*
+ * One decode step for sequences 0 .. n_seq-1 of the handle together (batched
+ * serving: independent streams, bitmaps and buffers), in two launches per 32
+ * sequences: the state updates of all of them (one cluster each), then one
+ * fused gather + projection + top-k over all their tiles (the grouped
+ * projection n_seq x [n x H] . [|I_t^b| x H]^T).  Results equal n_seq calls of
+ * ns_step, one per sequence, in order:
+ *   d_tree_ids       int32 [n_seq x n_tree]       sequence b's tree ids in row b
+ *   d_verify_logits  fp32  [n_seq x n_verify x V] sequence b's verify block
+ *   verify_rows      HOST int32 [n_seq]           the row of each block to rank
+ *   d_hidden         bf16  [n_seq x n x H]
+ *   d_logits         fp32  [n_seq x n x ld_logits] or NULL
+ *   d_topk_ids/vals        [n_seq x n x k]
+ * Every sequence must have been initialised (NS_ERR_STATE otherwise).
+ */
+NS_API ns_status ns_step_batch(ns_handle *h, int32_t n_seq, const int32_t *d_tree_ids, int32_t n_tree,
+                               const float *d_verify_logits, int32_t n_verify, const int32_t *verify_rows,
+                               const uint16_t *d_W_head, const uint16_t *d_hidden, int32_t n, int32_t k,
+                               float *d_logits, int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
+                               ns_stream stream);
+
+/*
  * The state half of ns_step in one launch: ns_stream_append followed by
  * ns_build_active_vocab (the "GPU-resident state update" that determines
  * I_{t+1}, MicroSpec §3.3).  Arguments as ns_stream_append.

@@ -31,6 +31,7 @@ struct ns_handle {
   int dense_ld = 0;
   cudaEvent_t trace[4] = {nullptr, nullptr, nullptr, nullptr};
   bool tracing = false;
+  long long seq_bytes = 0;  // distance between consecutive sequences' state
 };
 
 namespace {
@@ -154,6 +155,8 @@ ns_status ns_create(const ns_config *cfg, ns_handle **out) {
   }
   Carver carve(h->base);
   layout(h, carve);
+  if (c.batch > 1)
+    h->seq_bytes = reinterpret_cast<char *>(h->seqs[1].ring) - reinterpret_cast<char *>(h->seqs[0].ring);
   if (cudaMemset(h->base, 0, h->bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(h->base);
     delete h;
@@ -379,6 +382,68 @@ ns_status ns_step_slots(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, in
   if (e == cudaSuccess)
     e = enqueue_gather_project(h, seq, nullptr, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals, cs,
                                nullptr, true, Rows::kSlots);
+  return cuda_status(e);
+}
+
+ns_status ns_step_batch(ns_handle *h, int32_t n_seq, const int32_t *d_tree_ids, int32_t n_tree,
+                        const float *d_verify_logits, int32_t n_verify, const int32_t *verify_rows,
+                        const uint16_t *d_W_head, const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
+                        int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals, ns_stream stream) {
+  if (!h || n_seq < 1 || n_seq > h->cfg.batch) return NS_ERR_ARG;
+  if (n_tree < 0 || n_tree > h->cfg.max_tree || (n_tree > 0 && !d_tree_ids)) return NS_ERR_ARG;
+  const int V = h->cfg.V, H = h->cfg.H;
+  if (h->cfg.K_ver > 0) {
+    if (!d_verify_logits || n_verify < 1 || !verify_rows) return NS_ERR_ARG;
+    for (int b = 0; b < n_seq; ++b)
+      if (verify_rows[b] < 0 || verify_rows[b] >= n_verify) return NS_ERR_ARG;
+  }
+  if (!d_W_head || !aligned16(d_W_head)) return NS_ERR_ARG;
+  ns_status st = check_proj_args(h, d_hidden, n, k, d_logits, ld_logits, h->cfg.W_max, d_topk_ids, d_topk_vals);
+  if (st != NS_OK) return st;
+  for (int b = 0; b < n_seq; ++b)
+    if (!h->inited[b]) return NS_ERR_STATE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  for (int c0 = 0; c0 < n_seq && e == cudaSuccess; c0 += ns::kMaxBatchLaunch) {
+    const int nb = n_seq - c0 < ns::kMaxBatchLaunch ? n_seq - c0 : ns::kMaxBatchLaunch;
+    const ns::SeqDev &s0 = h->seqs[c0];
+    ns::StepBatch bt{};
+    bt.seq_bytes = h->seq_bytes;
+    bt.tree_stride = n_tree;
+    bt.z_stride = (long long)n_verify * V;
+    const float *verify = nullptr;
+    if (h->cfg.K_ver > 0) {
+      verify = d_verify_logits + (size_t)c0 * n_verify * V;
+      for (int b = 0; b < nb; ++b) bt.vrow[b] = verify_rows[c0 + b];
+    }
+    e = ns::launch_append_batch(s0, h->dims, nb, n_tree > 0 ? d_tree_ids + (size_t)c0 * n_tree : d_tree_ids,
+                                n_tree, verify, bt, h->err, cs);
+    if (e != cudaSuccess) break;
+    ns::UmmaLaunch L{};
+    L.W = d_W_head;
+    L.V = V;
+    L.H = H;
+    L.hid = d_hidden + (size_t)c0 * n * H;
+    L.n = n;
+    L.packed = s0.packed;
+    L.W_max = h->cfg.W_max;
+    L.idx = s0.active;
+    L.count_ptr = s0.count;
+    L.k = k;
+    L.logits = d_logits ? d_logits + (size_t)c0 * n * ld_logits : s0.logits;
+    L.ld = d_logits ? ld_logits : h->dims.ld_scratch;
+    L.cand_k = s0.cand_k;
+    L.cand_i = s0.cand_i;
+    L.slice_ticket = s0.slice_ticket;
+    L.out_ids = d_topk_ids + (size_t)c0 * n * k;
+    L.out_vals = d_topk_vals + (size_t)c0 * n * k;
+    L.err = h->err;
+    L.programmatic = true;
+    L.nseq = nb;
+    L.seq_bytes = h->seq_bytes;
+    L.logits_bytes = d_logits ? (long long)n * ld_logits * 4 : h->seq_bytes;
+    e = ns::launch_umma_step(L, cs);
+  }
   return cuda_status(e);
 }
 

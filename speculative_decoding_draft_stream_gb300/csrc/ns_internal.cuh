@@ -51,6 +51,36 @@ struct SeqDev {
 struct Dims {
   int32_t V, H, W_max, K_pre, K_ver, nwords, nwords_pad, ld_scratch;
   int32_t state_cluster;  // CTAs of the state-update cluster (16 where the device allows, else 8)
+  int32_t state_max16, state_max8;  // state-update clusters of 16 and of 8 CTAs resident at once
+};
+
+// The handle lays every sequence's state out identically, one sequence after
+// the other, so sequence b's buffers are sequence 0's moved by b * stride
+// bytes.  Null pointers (buffers a configuration does not have) stay null.
+template <typename T>
+__host__ __device__ inline void move_ptr(T *&p, long long off) {
+  if (p) p = reinterpret_cast<T *>(reinterpret_cast<char *>(p) + off);
+}
+__host__ __device__ inline SeqDev seq_at(SeqDev s, long long off) {
+  move_ptr(s.ring, off), move_ptr(s.counts, off), move_ptr(s.bitmap, off), move_ptr(s.active, off);
+  move_ptr(s.count, off), move_ptr(s.length, off), move_ptr(s.packed, off), move_ptr(s.logits, off);
+  move_ptr(s.first, off), move_ptr(s.cand, off), move_ptr(s.sinit, off), move_ptr(s.cand_k, off);
+  move_ptr(s.cand_i, off), move_ptr(s.slice_ticket, off), move_ptr(s.slot_id, off), move_ptr(s.held, off);
+  move_ptr(s.slot_meta, off), move_ptr(s.new_slot, off), move_ptr(s.new_id, off), move_ptr(s.slot_rows, off);
+  return s;
+}
+
+// One batched launch covers up to kMaxBatchLaunch consecutive sequences.
+constexpr int kMaxBatchLaunch = 32;
+
+// Where sequence b (0-based within the launch) finds its step inputs: state
+// at seq_at(s, b * seq_bytes), tree ids at tree + b * tree_stride, verify row
+// at verify + b * z_stride + vrow[b] * V.
+struct StepBatch {
+  long long seq_bytes;
+  long long z_stride;
+  int32_t tree_stride;
+  int32_t vrow[kMaxBatchLaunch];
 };
 
 // ---------------------------------------------------------------------------
@@ -318,6 +348,10 @@ cudaError_t launch_init(const SeqDev &s, const Dims &d, const int32_t *prompt, i
                         uint32_t *err, cudaStream_t st);
 cudaError_t launch_append(const SeqDev &s, const Dims &d, const int32_t *tree, int n_tree,
                           const float *verify_row_ptr, bool build, uint32_t *err, cudaStream_t st);
+// The state update (append + active vocabulary) of nseq <= kMaxBatchLaunch
+// sequences in one launch, one cluster per sequence; s is the first one's.
+cudaError_t launch_append_batch(const SeqDev &s, const Dims &d, int nseq, const int32_t *tree, int n_tree,
+                                const float *verify, const StepBatch &bt, uint32_t *err, cudaStream_t st);
 // Sets the state kernels' shared-memory limits and picks d->state_cluster.
 cudaError_t prepare_state_kernels(Dims *d);
 cudaError_t launch_build(const SeqDev &s, const Dims &d, uint32_t *err, cudaStream_t st);
@@ -369,6 +403,11 @@ struct UmmaLaunch {
   uint32_t *err;
   bool programmatic;         // may start while the preceding kernel finishes
   bool in_place;             // rows already in a contiguous buffer W (row j = id idx[j], -1 = skip), not stored
+  // nseq > 1: consecutive sequences in one launch (gather mode only); hid is
+  // [nseq x n x H], the per-sequence buffers above are sequence 0's and move
+  // by seq_bytes per sequence, logits by logits_bytes, outputs by n * k
+  int32_t nseq;
+  long long seq_bytes, logits_bytes;
 };
 int umma_tiles(int W_max);
 int umma_cluster();

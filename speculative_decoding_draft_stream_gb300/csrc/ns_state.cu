@@ -298,8 +298,11 @@ constexpr int kMaxCand = NS_MAX_SELECT_K * kRankPer;   // a pass's threshold can
 constexpr int kStateWarps = kStateThreads / kWarp;
 constexpr int kHashSlots = 256;                        // >= the most distinct ids one step touches
 
-template <bool VEC, bool BUILD>
-__global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims d, const int32_t *tree, int n_tree, const float *zrow, uint32_t *err) {
+// BATCH: one cluster per sequence; cluster b steps sequence b of the launch
+// (its state, tree ids and verify row located through `bt`).
+template <bool VEC, bool BUILD, bool BATCH>
+__global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims d, const int32_t *tree, int n_tree,
+                                                                  const float *zrow, uint32_t *err, StepBatch bt) {
   extern __shared__ uint4 s_dyn4[];  // leader: the bitmap and the nonzero-word list (nwords_pad words each)
   __shared__ uint32_t wl_k[kStateWarps * NS_MAX_SELECT_K], wl_i[kStateWarps * NS_MAX_SELECT_K];
   __shared__ uint32_t cand_k[NS_MAX_SELECT_K + kMaxCand], cand_i[NS_MAX_SELECT_K + kMaxCand];
@@ -326,6 +329,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
   const uint32_t rank = state_cluster_rank();
   const int nct = state_cluster_size();
   const bool leader = rank == 0;
+  if (BATCH) {
+    const int b = (int)(blockIdx.x / nct);
+    s = seq_at(s, b * bt.seq_bytes);
+    tree += (long long)b * bt.tree_stride;
+    if (zrow) zrow += b * bt.z_stride + (long long)bt.vrow[b] * d.V;
+  }
   uint32_t *s_bits = reinterpret_cast<uint32_t *>(s_dyn4);
   int32_t *s_nzw = reinterpret_cast<int32_t *>(s_bits + d.nwords_pad);
   int32_t *s_nzo = s_nzw + d.nwords_pad;
@@ -731,34 +740,38 @@ cudaError_t launch_prefill_topk(const SeqDev &s, const Dims &d, const float *Z, 
   return cudaGetLastError();
 }
 
-template <bool VEC, bool BUILD>
+template <bool VEC, bool BUILD, bool BATCH = false>
 cudaError_t launch_append_k(const SeqDev &s, const Dims &d, const int32_t *tree, int n_tree, const float *zrow,
-                            uint32_t *err, cudaStream_t st) {
+                            uint32_t *err, cudaStream_t st, const StepBatch &bt = StepBatch{}, int nseq = 1,
+                            int cluster = 0) {
+  if (cluster == 0) cluster = d.state_cluster;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(d.state_cluster, 1, 1);
+  cfg.gridDim = dim3(cluster * nseq, 1, 1);
   cfg.blockDim = dim3(kStateThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)state_smem_words(d.nwords_pad) * 4;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = d.state_cluster;
+  attr[0].val.clusterDim.x = cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, append_kernel<VEC, BUILD>, s, d, tree, n_tree, zrow, err);
+  return cudaLaunchKernelEx(&cfg, append_kernel<VEC, BUILD, BATCH>, s, d, tree, n_tree, zrow, err, bt);
 }
 
-template <bool VEC, bool BUILD>
+template <bool VEC, bool BUILD, bool BATCH = false>
 cudaError_t allow_append(int bytes) {
-  cudaError_t e = cudaFuncSetAttribute(append_kernel<VEC, BUILD>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(append_kernel<VEC, BUILD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e =
+      cudaFuncSetAttribute(append_kernel<VEC, BUILD, BATCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(append_kernel<VEC, BUILD, BATCH>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
 }
 
-// Whether a cluster of `n` append CTAs with `bytes` of dynamic shared memory
-// can be resident on this device.
-bool cluster_fits(int n, int bytes) {
+// How many clusters of `n` append CTAs with `bytes` of dynamic shared memory
+// can be resident at once on this device.
+int resident_clusters(int n, int bytes) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n, 1, 1);
   cfg.blockDim = dim3(kStateThreads, 1, 1);
@@ -771,13 +784,15 @@ bool cluster_fits(int n, int bytes) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  const cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, append_kernel<true, true>, &cfg);
+  const cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, append_kernel<true, true, false>, &cfg);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    return false;
+    return 0;
   }
-  return clusters >= 1;
+  return clusters;
 }
+
+bool cluster_fits(int n, int bytes) { return resident_clusters(n, bytes) >= 1; }
 
 }  // namespace
 
@@ -814,11 +829,14 @@ cudaError_t prepare_state_kernels(Dims *d) {
   cudaError_t e = cudaSuccess;
   const cudaError_t r[] = {allow_append<true, true>(bytes), allow_append<true, false>(bytes),
                            allow_append<false, true>(bytes), allow_append<false, false>(bytes),
+                           allow_append<true, true, true>(bytes), allow_append<false, true, true>(bytes),
                            cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)};
   for (cudaError_t x : r)
     if (x != cudaSuccess) e = x;
   if (e != cudaSuccess) return e;
-  d->state_cluster = cluster_fits(kMaxStateCluster, bytes) ? kMaxStateCluster : 8;
+  d->state_max16 = resident_clusters(kMaxStateCluster, bytes);
+  d->state_max8 = resident_clusters(8, bytes);
+  d->state_cluster = d->state_max16 >= 1 ? kMaxStateCluster : 8;
   return cluster_fits(d->state_cluster, bytes) ? cudaSuccess : cudaErrorNotSupported;
 }
 
@@ -831,6 +849,18 @@ cudaError_t launch_append(const SeqDev &s, const Dims &d, const int32_t *tree, i
   }
   return build ? launch_append_k<false, true>(s, d, tree, n_tree, zrow, err, st)
                : launch_append_k<false, false>(s, d, tree, n_tree, zrow, err, st);
+}
+
+cudaError_t launch_append_batch(const SeqDev &s, const Dims &d, int nseq, const int32_t *tree, int n_tree,
+                                const float *verify, const StepBatch &bt, uint32_t *err, cudaStream_t st) {
+  if (nseq < 1 || nseq > kMaxBatchLaunch) return cudaErrorInvalidValue;
+  // 16-CTA clusters rank faster, but take whichever size needs fewer waves
+  const int w16 = d.state_max16 > 0 ? (nseq + d.state_max16 - 1) / d.state_max16 : 1 << 30;
+  const int w8 = d.state_max8 > 0 ? (nseq + d.state_max8 - 1) / d.state_max8 : 1 << 30;
+  const int cluster = w16 <= w8 ? kMaxStateCluster : 8;
+  const bool vec = d.K_ver > 0 && (d.V % 4 == 0) && (reinterpret_cast<uintptr_t>(verify) % 16 == 0);
+  return vec ? launch_append_k<true, true, true>(s, d, tree, n_tree, verify, err, st, bt, nseq, cluster)
+             : launch_append_k<false, true, true>(s, d, tree, n_tree, verify, err, st, bt, nseq, cluster);
 }
 
 cudaError_t launch_build(const SeqDev &s, const Dims &d, uint32_t *err, cudaStream_t st) {

@@ -93,6 +93,20 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src,
                "r"(src), "r"(c0), "r"(c1)
                : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, int c0, int c1, int c2,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -183,6 +197,12 @@ struct UmmaArgs {
   int32_t *out_ids;          // [n x k]
   float *out_vals;
   uint32_t *err;
+  // kBatch: nseq sequences of tiles_per_seq tiles (of W_max) each; sequence
+  // b's state (idx, count, candidates, tickets) is b * seq_bytes past
+  // sequence 0's, its logits b * logits_bytes past, its outputs b * n * k
+  // entries past
+  long long seq_bytes, logits_bytes;
+  int32_t nseq, tiles_per_seq;
 };
 
 // kInPlace: the rows come from a contiguous buffer that already holds them
@@ -190,7 +210,11 @@ struct UmmaArgs {
 // tile is buffer row row0 + j, read in place and not stored back, and the
 // top-k maps row j to the id idx[j], skipping rows whose id is -1 (free slots;
 // count_ptr is then the slot table's high-water mark).
-template <int kUCluster, bool kInPlace>
+//
+// kBatch: one launch for several sequences (the hidden and packed tensor maps
+// get a third, per-sequence dimension); the clusters loop over the work items
+// (a tile of a sequence), see below.
+template <int kUCluster, bool kInPlace, bool kBatch = false>
 __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2)
     umma_step_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmP,
                      UmmaArgs a) {
@@ -209,8 +233,13 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = cluster_rank();
-  // clusters take tiles tile0, tile0 + ncl, ... (one each when the grid holds them all)
-  const int tile0 = blockIdx.x / kUCluster, ncl = gridDim.x / kUCluster;
+  // One sequence: clusters take tiles cid, cid + ncid, ... (one each when the
+  // grid holds them all).  kBatch: clusters take work items cid, cid + ncid,
+  // ... of nseq * tiles_per_seq; item i is tile i / nseq of sequence i % nseq
+  // (tile-major, so the tiles that exist come first), and the items past a
+  // sequence's |I_t| are skipped.
+  const int cid = blockIdx.x / kUCluster, ncid = gridDim.x / kUCluster;
+  __shared__ int s_cnt[kMaxBatchLaunch];  // kBatch: |I_t| of every sequence
 
   // ---- prologue (overlaps the state update when launched programmatically) --
   if (tid == 0) {
@@ -232,21 +261,30 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
   grid_dependency_wait();  // I_t and |I_t| come from the state update
   // The first tile's row ids load together with |I_t| (one round trip); the
   // entries past |I_t| are not used.
-  int id_first = 0;
-  if (tid < kUM && tile0 * kUM + tid < a.W_max) id_first = a.idx[tile0 * kUM + tid];
-  const int m = *a.count_ptr;
-  const int T = (m + kUM - 1) / kUM;
-  if (tile0 >= T) {  // uniform across the cluster
-    if (T == 0 && tile0 == 0) {
-      const int r = (int)crank * kSlice + warp;
-      if (warp < kSlice && r < a.n && lane < a.k) {
-        a.out_ids[r * a.k + lane] = -1;
-        a.out_vals[r * a.k + lane] = -__int_as_float(0x7f800000);
+  int id_first = 0, m0 = 0, T0 = 0;
+  if (kBatch) {
+    const int t0 = cid / a.nseq, b0 = cid % a.nseq;
+    const int32_t *idx0 = reinterpret_cast<const int32_t *>(reinterpret_cast<const char *>(a.idx) + b0 * a.seq_bytes);
+    if (tid < kUM && t0 * kUM + tid < a.W_max) id_first = idx0[t0 * kUM + tid];
+    if (tid < a.nseq)
+      s_cnt[tid] = *reinterpret_cast<const int32_t *>(reinterpret_cast<const char *>(a.count_ptr) + tid * a.seq_bytes);
+    __syncthreads();
+  } else {
+    if (tid < kUM && cid * kUM + tid < a.W_max) id_first = a.idx[cid * kUM + tid];
+    m0 = *a.count_ptr;
+    T0 = (m0 + kUM - 1) / kUM;
+    if (cid >= T0) {  // uniform across the cluster
+      if (T0 == 0 && cid == 0) {
+        const int r = (int)crank * kSlice + warp;
+        if (warp < kSlice && r < a.n && lane < a.k) {
+          a.out_ids[r * a.k + lane] = -1;
+          a.out_vals[r * a.k + lane] = -__int_as_float(0x7f800000);
+        }
       }
+      __syncwarp();
+      if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+      return;
     }
-    __syncwarp();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-    return;
   }
 
   const int KC = a.H / kUK;
@@ -254,12 +292,45 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
   const int nk = KC > (int)crank ? (KC - (int)crank + kUCluster - 1) / kUCluster : 0;
   // Stage use g = iter * nk + kt runs on across tiles: ring slot g % kUStages,
   // mbarrier phase g / kUStages.
-  for (int tile = tile0, iter = 0; tile < T; tile += ncl, ++iter) {
+  int iter = 0;  // work items processed so far
+  for (int item = cid;; item += ncid) {
+  int tile, bseq = 0, m, T;
+  if (kBatch) {
+    if (item >= a.nseq * a.tiles_per_seq) break;
+    tile = item / a.nseq;
+    bseq = item % a.nseq;
+    m = s_cnt[bseq];
+    T = (m + kUM - 1) / kUM;
+  } else {
+    tile = item;
+    m = m0;
+    T = T0;
+    if (tile >= T) break;
+  }
+  // this sequence's state and outputs
+  const long long so = bseq * a.seq_bytes;
+  const int32_t *idx = reinterpret_cast<const int32_t *>(reinterpret_cast<const char *>(a.idx) + so);
+  uint32_t *cand_k = reinterpret_cast<uint32_t *>(reinterpret_cast<char *>(a.cand_k) + so);
+  uint32_t *cand_i = reinterpret_cast<uint32_t *>(reinterpret_cast<char *>(a.cand_i) + so);
+  int32_t *ticket = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(a.slice_ticket) + so);
+  float *logits = reinterpret_cast<float *>(reinterpret_cast<char *>(a.logits) + bseq * a.logits_bytes);
+  int32_t *out_ids = a.out_ids + (long long)bseq * a.n * a.k;
+  float *out_vals = a.out_vals + (long long)bseq * a.n * a.k;
+  if (kBatch && tile >= T) {  // uniform across the cluster
+    if (T == 0 && tile == 0) {  // an empty I_t: padding only
+      const int r = (int)crank * kSlice + warp;
+      if (warp < kSlice && r < a.n && lane < a.k) {
+        out_ids[r * a.k + lane] = -1;
+        out_vals[r * a.k + lane] = -__int_as_float(0x7f800000);
+      }
+    }
+    continue;
+  }
   const int row0 = tile * kUM;
   if (tid < kUM) {
     const int j = row0 + tid;
     if (j < m) {
-      int id = iter == 0 ? id_first : a.idx[j];
+      int id = item == cid ? id_first : idx[j];
       if (kInPlace) {
         if (id < -1 || id >= a.V) {  // a row holds a valid id or is a free slot (-1)
           atomicOr(a.err, NS_FLAG_INTERNAL | (3u << 8));
@@ -288,7 +359,11 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
       if (g >= kUStages && !mbar_wait(bar_empty + 8 * s, ((g / kUStages) - 1) & 1, a.err)) break;
       issued = kt + 1;
       mbar_expect_tx(bar_full + 8 * s, kStageB);
-      tma_load_2d(base + s * kStage + kStageA, &tmH, ((int)crank + kt * kUCluster) * kUK, 0, bar_full + 8 * s);
+      if (kBatch)
+        tma_load_3d(base + s * kStage + kStageA, &tmH, ((int)crank + kt * kUCluster) * kUK, 0, bseq,
+                    bar_full + 8 * s);
+      else
+        tma_load_2d(base + s * kStage + kStageA, &tmH, ((int)crank + kt * kUCluster) * kUK, 0, bar_full + 8 * s);
     }
     // nothing may still be landing in shared memory when the CTA leaves
     const int first = issued > kUStages ? issued - kUStages : 0;
@@ -343,7 +418,10 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
     for (int kt = 0; kt < nk; ++kt) {
       const int g = iter * nk + kt, s = g % kUStages;
       if (!mbar_wait(bar_full + 8 * s, (g / kUStages) & 1, a.err)) break;
-      tma_store_2d(&tmP, base + s * kStage, ((int)crank + kt * kUCluster) * kUK, row0);
+      if (kBatch)
+        tma_store_3d(&tmP, base + s * kStage, ((int)crank + kt * kUCluster) * kUK, row0, bseq);
+      else
+        tma_store_2d(&tmP, base + s * kStage, ((int)crank + kt * kUCluster) * kUK, row0);
       bulk_commit();
       if (kt + 1 - released > kStoresInFlight) {  // the oldest store has read its stage
         asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kStoresInFlight) : "memory");
@@ -417,22 +495,22 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
       hi[q] = hk[q] != 0u ? (uint32_t)(kInPlace ? s_ids[j] : s_rows[j]) : (uint32_t)kEmptyId;
     }
     const size_t o = ((size_t)tile * kUN + r) * a.k;
-    warp_topk4(hk, hi, a.k, a.cand_k + o, a.cand_i + o);
+    warp_topk4(hk, hi, a.k, cand_k + o, cand_i + o);
   }
   __syncthreads();  // every warp's candidates are written before the ticket is taken
   if (tid == 0) {   // release this CTA's candidates; the last CTA acquires everyone's
     int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.slice_ticket + crank) : "memory");
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(ticket + crank) : "memory");
     *s_flag = old == T - 1;
   }
   for (int i = tid; i < kSlice * kUM; i += kUThreads) {
     const int rr = i / kUM, j = i % kUM;
     const int rw = (int)crank * kSlice + rr, jg = row0 + j;
-    if (rw < a.n && jg < m) a.logits[(size_t)rw * a.ld + jg] = F[i];
+    if (rw < a.n && jg < m) logits[(size_t)rw * a.ld + jg] = F[i];
   }
   __syncthreads();
   if (*s_flag) {  // last tile of this row slice: merge every tile's sorted candidates
-    if (tid == 0) a.slice_ticket[crank] = 0;
+    if (tid == 0) ticket[crank] = 0;
     if (row_warp) {
       const int K = a.k;
       uint32_t *ep = reinterpret_cast<uint32_t *>(gbase + kPartBytes + kSlice * kUM * 4);
@@ -455,8 +533,8 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
           for (int b = 0; b < kMergeBatch; ++b) {
             if (e0 + b * kWarp + lane < ne) {
               const size_t src = ((size_t)(t0 + l) * kUN + r) * K + q;
-              bk[b] = __ldcg(a.cand_k + src);
-              bi[b] = __ldcg(a.cand_i + src);
+              bk[b] = __ldcg(cand_k + src);
+              bi[b] = __ldcg(cand_i + src);
             }
             q += dq;
             l += dl;
@@ -484,14 +562,15 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
       }
       if (lane < K) {
         const uint32_t k = Rk[lane];
-        a.out_ids[r * K + lane] = k != 0u ? (int)Ri[lane] : -1;
-        a.out_vals[r * K + lane] = k != 0u ? key_value(k) : -__int_as_float(0x7f800000);
+        out_ids[r * K + lane] = k != 0u ? (int)Ri[lane] : -1;
+        out_vals[r * K + lane] = k != 0u ? key_value(k) : -__int_as_float(0x7f800000);
       }
     }
   }
   __syncwarp();
   cluster_sync();  // peers may still be reading this CTA's partial tile
-  }  // tiles
+  ++iter;
+  }  // work items
   if (!kInPlace && warp == 2 && lane == 0) bulk_wait_all();  // the packed-buffer stores are complete before the CTA leaves
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
@@ -523,6 +602,21 @@ bool encode_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t ou
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 tensor [outer x mid x inner]: rows of `inner` elements, `mid` rows
+// per block, blocks `outer_stride` bytes apart; 128-byte swizzle.
+bool encode_bf16_3d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t mid, uint64_t outer,
+                    uint64_t outer_stride, uint32_t box_inner, uint32_t box_mid) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {inner, mid, outer};
+  cuuint64_t strides[2] = {inner * 2, outer_stride};
+  cuuint32_t box[3] = {box_inner, box_mid, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -562,11 +656,12 @@ int max_clusters() {
   return clusters;
 }
 
-template <int CL, bool SLOTS>
+template <int CL, bool IN_PLACE, bool BATCH = false>
 cudaError_t allow_umma() {
-  cudaError_t e = cudaFuncSetAttribute(umma_step_kernel<CL, SLOTS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
+  cudaError_t e = cudaFuncSetAttribute(umma_step_kernel<CL, IN_PLACE, BATCH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
   if (e == cudaSuccess && CL > 8)
-    e = cudaFuncSetAttribute(umma_step_kernel<CL, SLOTS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(umma_step_kernel<CL, IN_PLACE, BATCH>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
 }
 
@@ -575,6 +670,8 @@ cudaError_t prepare_umma_kernels() {
   if (e == cudaSuccess) e = allow_umma<16, false>();
   if (e == cudaSuccess) e = allow_umma<8, true>();
   if (e == cudaSuccess) e = allow_umma<16, true>();
+  if (e == cudaSuccess) e = allow_umma<8, false, true>();
+  if (e == cudaSuccess) e = allow_umma<16, false, true>();
   if (e != cudaSuccess) return e;
   if (!encoder()) return cudaErrorNotSupported;
   g_max16 = max_clusters<16>();
@@ -583,9 +680,14 @@ cudaError_t prepare_umma_kernels() {
 }
 
 cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
+  const bool batch = L.nseq > 1;
+  if (L.in_place && batch) return cudaErrorInvalidValue;
   CUtensorMap tmH, tmP;
-  if (!encode_bf16_2d(&tmH, L.hid, L.H, L.n, kUK, kUN) || !encode_bf16_2d(&tmP, L.packed, L.H, L.W_max, kUK, kUM))
-    return cudaErrorInvalidValue;
+  const bool maps =
+      batch ? encode_bf16_3d(&tmH, L.hid, L.H, L.n, L.nseq, (uint64_t)L.n * L.H * 2, kUK, kUN) &&
+                  encode_bf16_3d(&tmP, L.packed, L.H, L.W_max, L.nseq, (uint64_t)L.seq_bytes, kUK, kUM)
+            : encode_bf16_2d(&tmH, L.hid, L.H, L.n, kUK, kUN) && encode_bf16_2d(&tmP, L.packed, L.H, L.W_max, kUK, kUM);
+  if (!maps) return cudaErrorInvalidValue;
   UmmaArgs a{};
   a.W = L.W;
   a.idx = L.idx;
@@ -603,9 +705,18 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   a.out_ids = L.out_ids;
   a.out_vals = L.out_vals;
   a.err = L.err;
+  const int nseq = batch ? L.nseq : 1;
+  a.seq_bytes = L.seq_bytes;
+  a.logits_bytes = L.logits_bytes;
+  a.nseq = nseq;
+  a.tiles_per_seq = umma_tiles(L.W_max);
   cudaLaunchConfig_t cfg = {};
-  const int CL = umma_tiles(L.W_max) <= g_max16 || g_max8 == 0 ? 16 : 8;
-  cfg.gridDim = dim3((unsigned)(umma_tiles(L.W_max) * CL));
+  // one cluster per tile of W_max; a batch gets as many 8-CTA clusters as are
+  // resident at once, which loop over the work items (tiles of every sequence)
+  int clusters = umma_tiles(L.W_max) * nseq;
+  const int CL = clusters <= g_max16 || g_max8 == 0 ? 16 : 8;
+  if (batch && CL == 8 && clusters > g_max8) clusters = g_max8;
+  cfg.gridDim = dim3((unsigned)(clusters * CL));
   cfg.blockDim = dim3(kUThreads);
   cfg.dynamicSmemBytes = kUSmem;
   cfg.stream = st;
@@ -614,6 +725,10 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = L.programmatic ? 1 : 0;
+  if (batch) {
+    if (CL == 16) return cudaLaunchKernelEx(&cfg, umma_step_kernel<16, false, true>, tmH, tmP, a);
+    return cudaLaunchKernelEx(&cfg, umma_step_kernel<8, false, true>, tmH, tmP, a);
+  }
   if (L.in_place) {
     if (CL == 16) return cudaLaunchKernelEx(&cfg, umma_step_kernel<16, true>, tmH, tmP, a);
     return cudaLaunchKernelEx(&cfg, umma_step_kernel<8, true>, tmH, tmP, a);

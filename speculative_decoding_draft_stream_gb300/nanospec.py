@@ -34,7 +34,7 @@ EXPORTED = (
     "ns_build_active_vocab", "ns_gather_head_rows", "ns_sub_lm_head_logits_topk", "ns_step",
     "ns_dense_lm_head_topk", "ns_get_active", "ns_get_state", "ns_get_error", "ns_state_update",
     "ns_gather_sub_lm_head_topk", "ns_trace_events", "ns_dense_lm_head_topk_noalloc", "ns_gather_new_head_rows",
-    "ns_slot_lm_head_logits_topk", "ns_step_slots", "ns_get_slots",
+    "ns_slot_lm_head_logits_topk", "ns_step_slots", "ns_get_slots", "ns_step_batch",
 )
 NOALLOC_MAX_LOGITS = 1 << 20
 
@@ -86,6 +86,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "ns_slot_lm_head_logits_topk": (I32, [P, I32, U16P, I32, I32, P, I32, P, P, P]),
         "ns_step_slots": (I32, [P, I32, P, I32, P, I32, I32, U16P, U16P, I32, I32, P, I32, P, P, P]),
         "ns_get_slots": (I32, [P, I32] + [ctypes.POINTER(P)] * 5),
+        "ns_step_batch": (I32, [P, I32, P, I32, P, I32, ctypes.POINTER(I32), U16P, U16P, I32, I32, P, I32, P, P,
+                                P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -225,6 +227,28 @@ class Handle:
                                  _ptr(W_head, _BF16, "W_head"), _ptr(hidden, _BF16, "hidden"), n, k,
                                  _ptr(logits, torch.float32, "logits"), ld, _ptr(ids, torch.int32, "ids"),
                                  _ptr(vals, torch.float32, "vals"), _stream(stream)), "ns_step")
+        return ids, vals
+
+    def step_batch(self, tree_ids: Optional[torch.Tensor], verify_logits: Optional[torch.Tensor], verify_rows,
+                   W_head: torch.Tensor, hidden: torch.Tensor, k: int, logits: Optional[torch.Tensor] = None,
+                   ids: Optional[torch.Tensor] = None, vals: Optional[torch.Tensor] = None,
+                   stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        """ns_step_batch for sequences 0 .. B-1: tree_ids [B, n_tree], verify_logits [B, n_verify, V],
+        verify_rows (B ints), hidden [B, n, H]; returns ids, vals [B, n, k]."""
+        B, n = hidden.shape[0], hidden.shape[1]
+        n_tree = 0 if tree_ids is None else tree_ids.shape[1]
+        n_v = 0 if verify_logits is None else verify_logits.shape[1]
+        rows = (ctypes.c_int32 * B)(*[int(x) for x in verify_rows]) if verify_logits is not None else None
+        if ids is None:
+            ids = torch.empty((B, n, k), dtype=torch.int32, device=self.device)
+        if vals is None:
+            vals = torch.empty((B, n, k), dtype=torch.float32, device=self.device)
+        ld = logits.shape[-1] if logits is not None else 0
+        _check(self._lib.ns_step_batch(self._h, B, _ptr(tree_ids, torch.int32, "tree_ids"), n_tree,
+                                       _ptr(verify_logits, torch.float32, "verify_logits"), n_v, rows,
+                                       _ptr(W_head, _BF16, "W_head"), _ptr(hidden, _BF16, "hidden"), n, k,
+                                       _ptr(logits, torch.float32, "logits"), ld, _ptr(ids, torch.int32, "ids"),
+                                       _ptr(vals, torch.float32, "vals"), _stream(stream)), "ns_step_batch")
         return ids, vals
 
     def state_update(self, seq: int, tree_ids: Optional[torch.Tensor], verify_logits: Optional[torch.Tensor],
