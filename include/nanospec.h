@@ -71,7 +71,7 @@ typedef int32_t ns_status;
 typedef void *ns_stream; /* cudaStream_t */
 typedef void *ns_event;  /* cudaEvent_t  */
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define NS_MAX_SELECT_K 16 /* K_pre and K_ver                               */
 #define NS_MAX_TOPK 32     /* k of the sub-head top-k                       */
 #define NS_MAX_ROWS 64     /* hidden rows per projection call (draft nodes) */
