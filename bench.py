@@ -746,6 +746,62 @@ def run_ours(args):
         us_torch = graph_us(lambda: (torch.index_select(W_bf, 0, idx_m, out=sel),
                                      torch.matmul(hid_bf, sel.t(), out=sub), torch.topk(sub.float(), k, dim=1)))
         extra["pinned_point"]["torch_index_select_matmul_topk_us"] = us_torch
+        # the indexed product (W_head rows through I_t, nothing packed: the
+        # naive indexed GEMM of NanoSpec's ablation) on the same state
+        init()
+        extra["pinned_point"]["indexed_no_pack_us"] = graph_us(
+            lambda: (h.build_active_vocab(0),
+                     h.sub_lm_head_indexed_topk(0, W_d, hid_d[0], k, logits=logits, ids=ids, vals=vals)))
+
+        # the vocabulary policies of NanoSpec's ablation, as decode steps
+        # (timed like the headline: T2 steps from the initial state, graph
+        # of steps minus graph of flushes): Ctx-only appends nothing after
+        # the prefill, Ext-only starts from an empty stream
+        def policy_us(init_fn, step_fn, T2=64):
+            init_fn()
+            for t in range(3):
+                step_fn(t)
+            torch.cuda.synchronize()
+            gs = []
+            for with_steps in (True, False):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for t in range(T2):
+                        flush.zero_()
+                        if with_steps:
+                            step_fn(t)
+                gs.append(g)
+            ms = []
+            for g in gs:
+                init_fn()
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                torch.cuda.synchronize()
+                ms.append(a.elapsed_time(b))
+            return 1e3 * (ms[0] - ms[1]) / T2
+
+        hc = ns.Handle(V, H, cfg.W_max, cfg.K_pre, 0, max_tree=n, max_k=k, max_prompt=len(prompt))
+        try:
+            def ctx_init():
+                hc.stream_init(0, prompt_d, Z_d)
+                hc.build_active_vocab(0)
+
+            us_ctx = policy_us(ctx_init, lambda t: hc.step(0, None, None, 0, W_d, hid_d[t % T], k, logits=logits,
+                                                           ids=ids, vals=vals))
+        finally:
+            hc.close()
+
+        def ext_init():
+            h.stream_init(0, None, None)
+            h.build_active_vocab(0)
+
+        us_ext = policy_us(ext_init, step)
+        extra["policies"] = {"ctx_only_step_us": us_ctx, "ext_only_step_us": us_ext,
+                             "ctx_plus_ext_step_us": 1e3 * total_ms / K,
+                             "note": "64 steps from the initial state each; the headline averages 512"}
 
         # two-stream pipeline (MicroSpec §3.3): the gather of W_head[I_t, :] on a
         # copy stream while a stand-in draft backbone runs on the compute

@@ -114,9 +114,12 @@ NS_API int64_t ns_device_bytes(const ns_handle *h);
 /*
  * Prefill: S_init = prompt (+) tuple(union over i of T_Kpre(z_i))
  * (MicroSpec §3.2, stream-initialisation equation).
- *   d_prompt          int32 [L], 1 <= L <= max_prompt, ids in [0, V)
+ *   d_prompt          int32 [L], 0 <= L <= max_prompt, ids in [0, V); L = 0
+ *                     (d_prompt may then be NULL) starts an empty stream, so
+ *                     the vocabulary comes from decode-time candidates alone
+ *                     (the Ext-only ablation of NanoSpec's evaluation)
  *   d_prefill_logits  fp32 [L x V] row-major, row i = z_i (may be NULL when
- *                     K_pre == 0)
+ *                     K_pre == 0 or L == 0)
  * The union is deduplicated in first-occurrence order, position-major then
  * rank-minor (largest logit first, ties to the smaller id); prompt ids are
  * kept verbatim.  Only the last W_max entries of S_init are stored.  Resets
@@ -228,6 +231,19 @@ NS_API ns_status ns_gather_sub_lm_head_topk(ns_handle *h, int32_t seq, const uin
                                             const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
                                             int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
                                             ns_stream stream);
+
+/*
+ * The projection straight from W_head through I_t, with no packed copy: the
+ * "naive indexed GEMM" of NanoSpec's ablation (evaluation, Table 5), kept
+ * as a measured comparator.  The same tcgen05 kernel as
+ * ns_gather_sub_lm_head_topk reads each W_head[I_t[j], :] in place and
+ * stores nothing to the packed buffer.  Arguments and results as
+ * ns_gather_sub_lm_head_topk (the packed buffer is left as it was).
+ */
+NS_API ns_status ns_sub_lm_head_indexed_topk(ns_handle *h, int32_t seq, const uint16_t *d_W_head,
+                                             const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
+                                             int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
+                                             ns_stream stream);
 
 /*
  * Slot-stable packed buffer: the incremental reading of NanoSpec's

@@ -179,8 +179,8 @@ int64_t ns_device_bytes(const ns_handle *h) { return h ? (int64_t)h->bytes : 0; 
 
 ns_status ns_stream_init(ns_handle *h, int32_t seq, const int32_t *d_prompt, int32_t L,
                          const float *d_prefill_logits, ns_stream stream) {
-  if (!valid_seq(h, seq) || !d_prompt || L < 1 || L > h->cfg.max_prompt) return NS_ERR_ARG;
-  if (h->cfg.K_pre > 0 && !d_prefill_logits) return NS_ERR_ARG;
+  if (!valid_seq(h, seq) || L < 0 || L > h->cfg.max_prompt || (L > 0 && !d_prompt)) return NS_ERR_ARG;
+  if (h->cfg.K_pre > 0 && L > 0 && !d_prefill_logits) return NS_ERR_ARG;
   ns_status st = cuda_status(ns::launch_init(h->seqs[seq], h->dims, d_prompt, L, d_prefill_logits, h->err,
                                              static_cast<cudaStream_t>(stream)));
   if (st == NS_OK) h->inited[seq] = 1;
@@ -247,6 +247,7 @@ enum class Rows {
   kGather,  // W_head through I_t, storing them to the packed buffer on the way
   kPacked,  // the packed buffer, row j = I_t[j] (after a separate gather)
   kSlots,   // the slot buffer, row s = slot_id[s] (-1: free, not ranked)
+  kIndexed, // W_head rows through I_t, nothing packed (the indexed product)
 };
 
 // Projection + top-k (one tcgen05 kernel).  `mid` (nullable) is recorded
@@ -258,7 +259,7 @@ static cudaError_t enqueue_gather_project(ns_handle *h, int32_t seq, const uint1
                                           cudaEvent_t mid, bool programmatic, Rows rows = Rows::kGather) {
   const ns::SeqDev &s = h->seqs[seq];
   ns::UmmaLaunch L{};
-  L.W = rows == Rows::kGather ? d_W_head : rows == Rows::kPacked ? s.packed : s.slot_rows;
+  L.W = rows == Rows::kGather || rows == Rows::kIndexed ? d_W_head : rows == Rows::kPacked ? s.packed : s.slot_rows;
   L.V = h->cfg.V;
   L.H = h->cfg.H;
   L.hid = d_hidden;
@@ -268,6 +269,7 @@ static cudaError_t enqueue_gather_project(ns_handle *h, int32_t seq, const uint1
   L.idx = rows == Rows::kSlots ? s.slot_id : s.active;
   L.count_ptr = rows == Rows::kSlots ? s.slot_meta : s.count;
   L.in_place = rows != Rows::kGather;
+  L.rows_by_id = rows == Rows::kIndexed;
   L.k = k;
   L.logits = d_logits ? d_logits : s.logits;
   L.ld = d_logits ? ld_logits : h->dims.ld_scratch;
@@ -322,6 +324,17 @@ ns_status ns_gather_sub_lm_head_topk(ns_handle *h, int32_t seq, const uint16_t *
   if (st != NS_OK) return st;
   return cuda_status(enqueue_gather_project(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids,
                                             d_topk_vals, static_cast<cudaStream_t>(stream), nullptr, false));
+}
+
+ns_status ns_sub_lm_head_indexed_topk(ns_handle *h, int32_t seq, const uint16_t *d_W_head, const uint16_t *d_hidden,
+                                      int32_t n, int32_t k, float *d_logits, int32_t ld_logits, int32_t *d_topk_ids,
+                                      float *d_topk_vals, ns_stream stream) {
+  ns_status st = check_gather_project_args(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids,
+                                           d_topk_vals);
+  if (st != NS_OK) return st;
+  return cuda_status(enqueue_gather_project(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids,
+                                            d_topk_vals, static_cast<cudaStream_t>(stream), nullptr, false,
+                                            Rows::kIndexed));
 }
 
 ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,

@@ -408,6 +408,7 @@ struct UmmaLaunch {
   // by seq_bytes per sequence, logits by logits_bytes, outputs by n * k
   int32_t nseq;
   long long seq_bytes, logits_bytes;
+  bool rows_by_id;           // in_place over W_head itself: row j = W row idx[j]
 };
 int umma_tiles(int W_max);
 int umma_cluster();

@@ -801,7 +801,7 @@ cudaError_t launch_init(const SeqDev &s, const Dims &d, const int32_t *prompt, i
   const int n = reset_extent(d);
   init_reset_kernel<<<(n + 255) / 256, 256, 0, st>>>(s, d);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || L == 0) return e;  // an empty prompt leaves the stream empty
   if (d.K_pre > 0) {
     const bool vec = (d.V % 4 == 0) && (reinterpret_cast<uintptr_t>(prefill) % 16 == 0);
     const int K = d.K_pre;

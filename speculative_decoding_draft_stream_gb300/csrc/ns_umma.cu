@@ -203,13 +203,16 @@ struct UmmaArgs {
   // entries past
   long long seq_bytes, logits_bytes;
   int32_t nseq, tiles_per_seq;
+  int32_t rows_by_id;  // kInPlace: row j is W row idx[j] (an indexed product, nothing packed)
 };
 
-// kInPlace: the rows come from a contiguous buffer that already holds them
-// (the packed buffer after a separate gather, or the slot buffer): row j of a
-// tile is buffer row row0 + j, read in place and not stored back, and the
-// top-k maps row j to the id idx[j], skipping rows whose id is -1 (free slots;
-// count_ptr is then the slot table's high-water mark).
+// kInPlace: the rows come from a buffer that already holds them (the packed
+// buffer after a separate gather, or the slot buffer): row j of a tile is
+// buffer row row0 + j, read in place and not stored back, and the top-k maps
+// row j to the id idx[j], skipping rows whose id is -1 (free slots; count_ptr
+// is then the slot table's high-water mark).  With rows_by_id the buffer is
+// W_head itself and row j is W_head row idx[j]: the indexed product without a
+// packed copy.
 //
 // kBatch: one launch for several sequences (the hidden and packed tensor maps
 // get a third, per-sequence dimension); the clusters loop over the work items
@@ -337,7 +340,7 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 2
           id = -1;
         }
         s_ids[tid] = id;
-        s_rows[tid] = j;
+        s_rows[tid] = a.rows_by_id ? (id < 0 ? 0 : id) : j;  // rows_by_id: W_head rows, no packed copy
       } else {
         if ((unsigned)id >= (unsigned)a.V) {  // I_t only holds valid ids
           atomicOr(a.err, NS_FLAG_INTERNAL | (3u << 8));
@@ -710,6 +713,7 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   a.logits_bytes = L.logits_bytes;
   a.nseq = nseq;
   a.tiles_per_seq = umma_tiles(L.W_max);
+  a.rows_by_id = L.rows_by_id ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   // one cluster per tile of W_max; a batch gets as many 8-CTA clusters as are
   // resident at once, which loop over the work items (tiles of every sequence)

@@ -34,7 +34,7 @@ EXPORTED = (
     "ns_build_active_vocab", "ns_gather_head_rows", "ns_sub_lm_head_logits_topk", "ns_step",
     "ns_dense_lm_head_topk", "ns_get_active", "ns_get_state", "ns_get_error", "ns_state_update",
     "ns_gather_sub_lm_head_topk", "ns_trace_events", "ns_dense_lm_head_topk_noalloc", "ns_gather_new_head_rows",
-    "ns_slot_lm_head_logits_topk", "ns_step_slots", "ns_get_slots", "ns_step_batch",
+    "ns_slot_lm_head_logits_topk", "ns_step_slots", "ns_get_slots", "ns_step_batch", "ns_sub_lm_head_indexed_topk",
 )
 NOALLOC_MAX_LOGITS = 1 << 20
 
@@ -86,6 +86,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "ns_slot_lm_head_logits_topk": (I32, [P, I32, U16P, I32, I32, P, I32, P, P, P]),
         "ns_step_slots": (I32, [P, I32, P, I32, P, I32, I32, U16P, U16P, I32, I32, P, I32, P, P, P]),
         "ns_get_slots": (I32, [P, I32] + [ctypes.POINTER(P)] * 5),
+        "ns_sub_lm_head_indexed_topk": (I32, [P, I32, U16P, U16P, I32, I32, P, I32, P, P, P]),
         "ns_step_batch": (I32, [P, I32, P, I32, P, I32, ctypes.POINTER(I32), U16P, U16P, I32, I32, P, I32, P, P,
                                 P]),
     }
@@ -171,9 +172,13 @@ class Handle:
         return int(self._lib.ns_device_bytes(self._h))
 
     # -- the C ABI -------------------------------------------------------------
-    def stream_init(self, seq: int, prompt: torch.Tensor, prefill_logits: Optional[torch.Tensor],
+    def stream_init(self, seq: int, prompt: Optional[torch.Tensor], prefill_logits: Optional[torch.Tensor],
                     stream=None) -> None:
-        _check(self._lib.ns_stream_init(self._h, seq, _ptr(prompt, torch.int32, "prompt"), prompt.numel(),
+        """prompt None (or empty) starts an empty stream."""
+        L = 0 if prompt is None else prompt.numel()
+        if L == 0:
+            prompt = None
+        _check(self._lib.ns_stream_init(self._h, seq, _ptr(prompt, torch.int32, "prompt"), L,
                                         _ptr(prefill_logits, torch.float32, "prefill_logits"), _stream(stream)),
                "ns_stream_init")
 
@@ -316,6 +321,19 @@ class Handle:
         return (_view(p[0].value, (c.W_max,), "<i4", self.device), _view(p[1].value, (2,), "<i4", self.device),
                 _view(p[2].value, (c.W_max,), "<i4", self.device), _view(p[3].value, (c.W_max,), "<i4", self.device),
                 _view(p[4].value, (c.W_max, c.H), "<i2", self.device))
+
+    def sub_lm_head_indexed_topk(self, seq: int, W_head: torch.Tensor, hidden: torch.Tensor, k: int,
+                                 logits: Optional[torch.Tensor] = None, ids: Optional[torch.Tensor] = None,
+                                 vals: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        n = hidden.shape[0]
+        ids, vals = self._outputs(n, k, ids, vals)
+        ld = logits.shape[1] if logits is not None else 0
+        _check(self._lib.ns_sub_lm_head_indexed_topk(self._h, seq, _ptr(W_head, _BF16, "W_head"),
+                                                     _ptr(hidden, _BF16, "hidden"), n, k,
+                                                     _ptr(logits, torch.float32, "logits"), ld,
+                                                     _ptr(ids, torch.int32, "ids"), _ptr(vals, torch.float32, "vals"),
+                                                     _stream(stream)), "ns_sub_lm_head_indexed_topk")
+        return ids, vals
 
     def trace_events(self, events) -> None:
         """Record ns_step's kernel boundaries on four torch.cuda.Events (None: off)."""
