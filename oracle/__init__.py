@@ -32,4 +32,6 @@ from .nanospec_oracle import (  # noqa: F401
     top_k,
     top_k_rows,
     topk_remap,
+    union_sub_head_step,
+    union_vocab,
 )

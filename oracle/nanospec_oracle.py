@@ -56,6 +56,10 @@ Readings where the pages are silent (each also listed in the design notes):
    the free slots in ascending id order, lowest slot first.  The first update
    after the stream is initialised therefore lays I_1 out ascending, the same
    layout as the full repack.
+11. Batched shared gather (several sequences' sub-heads from one packed
+   buffer): the buffer holds the union U of the sequences' I_t, ascending;
+   each sequence projects through all of it and ranks only its own columns,
+   so its top-k is the one its own I_t gives.
 
 """
 
@@ -310,6 +314,39 @@ def slot_project_topk(hid_bits, rows_bits, slot_id, k: int):
     by_id = occ[np.argsort(slot_id[occ], kind="stable")]  # occupied slots, ids ascending
     ids, vals = topk_remap(logits[:, by_id], slot_id[by_id], k)
     return logits, ids, vals
+
+
+# ---------------------------------------------------------------------------
+# Batched shared gather [gather] over several sequences (reading 11)
+# ---------------------------------------------------------------------------
+def union_vocab(I_list):
+    """U = the union of the sequences' active sets, ascending, and the mask
+    M[b, j] = (U[j] in I_b) of which columns each sequence may rank."""
+    U = np.array(sorted(set(int(x) for I in I_list for x in I)), dtype=np.int32)
+    M = np.zeros((len(I_list), len(U)), dtype=bool)
+    pos = {int(x): j for j, x in enumerate(U.tolist())}
+    for b, I in enumerate(I_list):
+        for x in I:
+            M[b, pos[int(x)]] = True
+    return U, M
+
+
+def union_sub_head_step(hid_list, W_bits, I_list, k: int):
+    """One gather of W_head[U, :] for all sequences, every sequence's hidden
+    rows projected through it, and each sequence's top-k over its own columns
+    only.  Returns (U, M, packed [|U| x H], logits per sequence [n_b x |U|],
+    ids, vals per sequence)."""
+    U, M = union_vocab(I_list)
+    packed = gather_rows(W_bits, U)
+    logits, ids, vals = [], [], []
+    for b, hid in enumerate(hid_list):
+        z = project(hid, packed)
+        cols = np.flatnonzero(M[b])  # ascending, so ids ascend with the column
+        i_b, v_b = topk_remap(z[:, cols], U[cols], k)
+        logits.append(z)
+        ids.append(i_b)
+        vals.append(v_b)
+    return U, M, packed, logits, ids, vals
 
 
 class OracleSlots:
