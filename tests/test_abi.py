@@ -75,3 +75,33 @@ def test_create_rejects_bad_config_before_touching_the_gpu(lib_path):
     assert lib.ns_destroy(None) == -1
     assert lib.ns_stream_init(None, 0, None, 1, None, None) == -1
     assert lib.ns_get_error(None, None, 0) == -1
+
+
+def test_every_entry_point_rejects_a_null_handle(lib_path):
+    """Each call that takes a handle returns NS_ERR_ARG for NULL before
+    touching the GPU (the argument checks run on the host first)."""
+    from speculative_decoding_draft_stream_gb300.nanospec import load_library
+
+    lib = load_library(lib_path)
+    z = None
+    calls = {
+        "ns_stream_append": (z, 0, z, 0, z, 0, 0, z),
+        "ns_build_active_vocab": (z, 0, z),
+        "ns_gather_head_rows": (z, 0, z, z, z),
+        "ns_sub_lm_head_logits_topk": (z, 0, z, 1, 1, z, 0, z, z, z),
+        "ns_step": (z, 0, z, 0, z, 0, 0, z, z, 1, 1, z, 0, z, z, z),
+        "ns_state_update": (z, 0, z, 0, z, 0, 0, z),
+        "ns_gather_sub_lm_head_topk": (z, 0, z, z, 1, 1, z, 0, z, z, z),
+        "ns_sub_lm_head_indexed_topk": (z, 0, z, z, 1, 1, z, 0, z, z, z),
+        "ns_dense_lm_head_topk": (z, z, 1, z, 1, 1, z, 0, z, z, z),
+        "ns_gather_new_head_rows": (z, 0, z, z, z),
+        "ns_slot_lm_head_logits_topk": (z, 0, z, 1, 1, z, 0, z, z, z),
+        "ns_step_slots": (z, 0, z, 0, z, 0, 0, z, z, 1, 1, z, 0, z, z, z),
+        "ns_step_batch": (z, 1, z, 0, z, 0, z, z, z, 1, 1, z, 0, z, z, z),
+        "ns_get_active": (z, 0, z, z, z, z),
+        "ns_get_state": (z, 0, z, z, z),
+        "ns_get_slots": (z, 0, z, z, z, z, z),
+        "ns_trace_events": (z, z, 0),
+    }
+    for name, args in calls.items():
+        assert getattr(lib, name)(*args) == -1, name
