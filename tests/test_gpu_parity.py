@@ -1,8 +1,8 @@
 """GPU parity: the CUDA path through the C ABI against the CPU oracle.
 
 Small workloads are compared element by element on every step (state, packed
-sub-head, logits, top-k); they still span several 64-row tiles, K splits and
-ragged tails.  Edge cases cover the degenerate windows, empty appends, bad
+sub-head, logits, top-k); they still span several 128-row tiles of the fused
+kernel, H split over the CTAs of a cluster, and ragged tails.  Edge cases cover the degenerate windows, empty appends, bad
 ids, padding, the scalar (V % 4 != 0) paths and the largest K and k.
 """
 
@@ -94,7 +94,7 @@ def test_toy_every_step(pkg, fused):
     _run_workload(pkg, TOY, fused)
 
 
-# A mid-size head: several row tiles, a ragged last tile, K split 16 ways,
+# A mid-size head: several row tiles, a ragged last tile, H split over a cluster,
 # H = 1024 (16 k-slices) and V not a multiple of 32.
 MID = WorkloadConfig(name="mid", V=20011, H=1024, W_max=1000, K_pre=3, K_ver=3, prompt_len=700, self_copy=0.4,
                      zipf_s=1.05, steps=12, n_tree=60, tree_local=0.7, tree_recent=256, n_verify=4)
