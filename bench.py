@@ -202,6 +202,24 @@ def time_oracle(cfg, wl, steps_wanted: int, budget_s: float, warmup: int = 0):
     return done, dt
 
 
+def single_thread_oracle(workload: str, steps: int, timeout_s: float = 180.0):
+    """The reference arm's oracle sample in a child process limited to one
+    BLAS/OpenMP thread (the thread counts are read when numpy loads, so they
+    are set in the child's environment).  None when the child fails."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[v] = "1"
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", workload,
+           "--steps", str(steps), "--warmup", "0"]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=timeout_s)
+        line = [x for x in r.stdout.splitlines() if x.startswith("{")][-1]
+        d = json.loads(line)
+        return {"value": d["value"], "unit": d["unit"], "cores": 1, "sample": d["cpu_baseline"]["sample"]}
+    except (subprocess.SubprocessError, OSError, IndexError, ValueError, KeyError):
+        return None
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -869,7 +887,8 @@ def run_ours(args):
     if rank == 0 and world == 1:
         done, dt = time_oracle(cfg, wl, T, budget_s=args.cpu_seconds)
         cpu = {"value": done / dt, "unit": "steps/s", "cores": oracle_threads(), "kind": "oracle",
-               "sample": f"first {done} decode steps of {cfg.name} after its prefill init (prefill not timed)"}
+               "sample": f"first {done} decode steps of {cfg.name} after its prefill init (prefill not timed)",
+               "single_thread": single_thread_oracle(cfg.name, steps=16)}
 
     if rank == 0:
         mean_m = float(np.mean(m_list))

@@ -39,3 +39,8 @@ def test_step_bytes_count_rows_read_and_written():
     # rows read + packed written, logits, hiddens, one verify row, bitmap read and written, I_t
     assert bench.step_bytes(m, n, H, V) == 2 * m * H * 2 + n * m * 4 + n * H * 2 + V * 4 + 2 * 16032 + 4 * m
     assert bench.proj_bytes(m, n, H) == bench.step_bytes(m, n, H, V) - V * 4 - 2 * 16032
+
+
+def test_single_thread_oracle_sample():
+    d = bench.single_thread_oracle(bench.DEFAULT_WORKLOAD, steps=2)
+    assert d is not None and d["cores"] == 1 and d["value"] > 0 and d["unit"] == "steps/s"
