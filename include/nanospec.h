@@ -35,7 +35,10 @@
  *     ns_get_error.
  *   - Work for one sequence must be ordered (one stream, or events).  Work
  *     for different sequences may run concurrently.
- *   - Logits must be finite; the order among NaNs is undefined.
+ *   - Every Top-K and top-k orders by value, larger first, ties to the
+ *     smaller id; -0.0 ties +0.0; +inf and -inf are ordered like any value;
+ *     NaN never ranks (a row with fewer than K non-NaN values yields fewer
+ *     entries, see the calls).
  */
 #ifndef NANOSPEC_H
 #define NANOSPEC_H
@@ -183,13 +186,21 @@ NS_API ns_status ns_sub_lm_head_logits_topk(ns_handle *h, int32_t seq, const uin
  * One whole decode step for one sequence, in as few launches as the library
  * can: ns_stream_append, ns_build_active_vocab, the gather (writing the
  * packed buffer) and the projection with top-k, with the same arguments and
- * results as those calls made in order on `stream`.
+ * results as those calls made in order on `stream`.  Where the device holds
+ * the whole grid at once it is ONE cooperative launch (ns_step_launches
+ * returns 1): every CTA ranks a slice of the verify row, one grid barrier
+ * joins them, and each CTA then updates the window and compacts I_t for its
+ * own tiles before running them; otherwise it is ns_state_update followed by
+ * ns_gather_sub_lm_head_topk.
  */
 NS_API ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
                   const float *d_verify_logits, int32_t n_verify, int32_t verify_row,
                   const uint16_t *d_W_head, const uint16_t *d_hidden, int32_t n, int32_t k,
                   float *d_logits, int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
                   ns_stream stream);
+
+/* Kernel launches one ns_step makes on this handle (1 or 2; 0 for NULL). */
+NS_API int32_t ns_step_launches(const ns_handle *h);
 
 /*
  * One decode step for sequences 0 .. n_seq-1 of the handle together (batched

@@ -29,6 +29,9 @@ struct ns_handle {
   float *dense_part = nullptr;    // [pgrid x tile]
   int32_t *dense_tickets = nullptr;
   int dense_ld = 0;
+  int step_clusters = 0;  // clusters of the one-launch step (0: two launches)
+  int step_tpc = 0;       // tiles per cluster of the one-launch step
+  int step_cl = 0;        // CTAs per cluster of the one-launch step
   cudaEvent_t trace[4] = {nullptr, nullptr, nullptr, nullptr};
   bool tracing = false;
   long long seq_bytes = 0;  // distance between consecutive sequences' state
@@ -83,6 +86,9 @@ void layout(ns_handle *h, Carver &cv) {
     s.new_slot = cv.take<int32_t>(c.W_max);
     s.new_id = cv.take<int32_t>(c.W_max);
     s.slot_rows = cv.take<uint16_t>((size_t)c.W_max * c.H);
+    s.gbar = cv.take<unsigned long long>(1);
+    s.vcand_k = cv.take<uint32_t>((size_t)ns::kMaxStepCtas * (c.K_ver > 0 ? c.K_ver : 1));
+    s.vcand_i = cv.take<uint32_t>((size_t)ns::kMaxStepCtas * (c.K_ver > 0 ? c.K_ver : 1));
   }
   h->dense_ld = (c.V + 3) & ~3;
   h->dense_logits = cv.take<float>((size_t)ns::kProjBN * h->dense_ld);
@@ -124,7 +130,8 @@ ns_status ns_create(const ns_config *cfg, ns_handle **out) {
   h->cfg = c;
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
-      ns::prepare_project_kernels() != cudaSuccess || ns::prepare_umma_kernels() != cudaSuccess) {
+      ns::prepare_project_kernels() != cudaSuccess || ns::prepare_umma_kernels() != cudaSuccess ||
+      ns::prepare_step_kernel() != cudaSuccess) {
     delete h;
     return NS_ERR_CUDA;
   }
@@ -163,6 +170,22 @@ ns_status ns_create(const ns_config *cfg, ns_handle **out) {
     return NS_ERR_CUDA;
   }
   h->inited.assign(c.batch, 0);
+  // The one-launch step needs every CTA of its grid resident at once (a
+  // cooperative launch); check once that the device takes such a launch.
+  h->step_clusters = ns::step_plan(d, &h->step_tpc, &h->step_cl);
+  if (h->step_clusters > 0) {
+    ns::StepLaunch L{};
+    L.s = h->seqs[0];
+    L.d = d;
+    L.clusters = h->step_clusters;
+    L.tiles_per_cluster = h->step_tpc;
+    L.cluster_size = h->step_cl;
+    L.probe = true;
+    if (ns::launch_step(L, nullptr) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+      cudaGetLastError();
+      h->step_clusters = 0;
+    }
+  }
   *out = h;
   return NS_OK;
 }
@@ -176,6 +199,8 @@ ns_status ns_destroy(ns_handle *h) {
 }
 
 int64_t ns_device_bytes(const ns_handle *h) { return h ? (int64_t)h->bytes : 0; }
+
+int32_t ns_step_launches(const ns_handle *h) { return h ? (h->step_clusters > 0 ? 1 : 2) : 0; }
 
 ns_status ns_stream_init(ns_handle *h, int32_t seq, const int32_t *d_prompt, int32_t L,
                          const float *d_prefill_logits, ns_stream stream) {
@@ -349,6 +374,31 @@ ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t 
   const bool tr = h->tracing;
   cudaError_t e = tr ? trace_record(h->trace[0], cs) : cudaSuccess;
   const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
+  if (h->step_clusters > 0) {  // one launch: state update, gather, projection, top-k
+    if (e == cudaSuccess && tr) e = trace_record(h->trace[1], cs);
+    ns::StepLaunch L{};
+    L.s = h->seqs[seq];
+    L.d = h->dims;
+    L.W = d_W_head;
+    L.hid = d_hidden;
+    L.n = n;
+    L.k = k;
+    L.logits = d_logits ? d_logits : h->seqs[seq].logits;
+    L.ld = d_logits ? ld_logits : h->dims.ld_scratch;
+    L.out_ids = d_topk_ids;
+    L.out_vals = d_topk_vals;
+    L.err = h->err;
+    L.tree = d_tree_ids;
+    L.n_tree = n_tree;
+    L.zrow = zrow;
+    L.clusters = h->step_clusters;
+    L.tiles_per_cluster = h->step_tpc;
+    L.cluster_size = h->step_cl;
+    if (e == cudaSuccess) e = ns::launch_step(L, cs);
+    if (e == cudaSuccess && tr) e = trace_record(h->trace[2], cs);
+    if (e == cudaSuccess && tr) e = trace_record(h->trace[3], cs);
+    return cuda_status(e);
+  }
   if (e == cudaSuccess) e = ns::launch_append(h->seqs[seq], h->dims, d_tree_ids, n_tree, zrow, true, h->err, cs);
   if (e == cudaSuccess && tr) e = trace_record(h->trace[1], cs);
   if (e == cudaSuccess)

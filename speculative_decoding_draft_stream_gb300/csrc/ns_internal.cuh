@@ -46,6 +46,10 @@ struct SeqDev {
   int32_t *new_slot;    // [W_max] (slot, id) of each row the last update gathered, in assignment order
   int32_t *new_id;      // [W_max]
   uint16_t *slot_rows;  // [W_max x H] bf16 slot buffer
+  // one-launch step (ns_step.cu)
+  unsigned long long *gbar;  // [1] grid barrier counter (grows by the grid size per step)
+  uint32_t *vcand_k;         // [kMaxStepCtas x K_ver] each CTA's verify Top-K: order keys
+  uint32_t *vcand_i;         //   and ids
 };
 
 struct Dims {
@@ -67,6 +71,7 @@ __host__ __device__ inline SeqDev seq_at(SeqDev s, long long off) {
   move_ptr(s.first, off), move_ptr(s.cand, off), move_ptr(s.sinit, off), move_ptr(s.cand_k, off);
   move_ptr(s.cand_i, off), move_ptr(s.slice_ticket, off), move_ptr(s.slot_id, off), move_ptr(s.held, off);
   move_ptr(s.slot_meta, off), move_ptr(s.new_slot, off), move_ptr(s.new_id, off), move_ptr(s.slot_rows, off);
+  move_ptr(s.gbar, off), move_ptr(s.vcand_k, off), move_ptr(s.vcand_i, off);
   return s;
 }
 
@@ -213,6 +218,7 @@ __device__ __forceinline__ void warp_merge_lists(const uint32_t *lk, const uint3
   int p = 0;
   lastk = 0u;
   lasti = (uint32_t)kEmptyId;
+#pragma unroll 1  // code size: these loops run once per call
   for (int r = 0; r < K; ++r) {
     uint32_t hk = 0u, hi = (uint32_t)kEmptyId;
     if (lane < nl && p < K) {
@@ -257,6 +263,7 @@ __device__ __forceinline__ void sort4_desc(uint32_t *k, uint32_t *i) {
 __device__ __forceinline__ void warp_topk4(uint32_t *hk, uint32_t *hi, int K, uint32_t *ok, uint32_t *oi) {
   const int lane = threadIdx.x & (kWarp - 1);
   sort4_desc(hk, hi);
+#pragma unroll 1  // code size: these loops run once per call
   for (int r = 0; r < K; ++r) {
     uint32_t bk, bi;
     warp_best(hk[0], hi[0], bk, bi);
@@ -278,11 +285,39 @@ __device__ __forceinline__ void warp_topk4(uint32_t *hk, uint32_t *hi, int K, ui
   __syncwarp();
 }
 
+// warp_topk4 on two independent sets of four pairs per lane at once (their
+// rounds overlap), with the winners kept in registers: lane r ends with
+// winner r (r < K) of each set, so each set's K entries leave in one
+// coalesced store.
+__device__ __forceinline__ void warp_topk4_pair(uint32_t *ka, uint32_t *ia, uint32_t *kb, uint32_t *ib, int K,
+                                                uint32_t *wak, uint32_t *wai, uint32_t *wbk, uint32_t *wbi) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  sort4_desc(ka, ia);
+  sort4_desc(kb, ib);
+  *wak = 0u, *wai = (uint32_t)kEmptyId, *wbk = 0u, *wbi = (uint32_t)kEmptyId;
+  auto pop = [](uint32_t *k, uint32_t *i) {
+    k[0] = k[1], i[0] = i[1], k[1] = k[2], i[1] = i[2], k[2] = k[3], i[2] = i[3];
+    k[3] = 0u, i[3] = (uint32_t)kEmptyId;
+  };
+#pragma unroll 1  // code size: these loops run once per call
+  for (int r = 0; r < K; ++r) {
+    uint32_t ak, ai, bk, bi;
+    warp_best(ka[0], ia[0], ak, ai);
+    warp_best(kb[0], ib[0], bk, bi);
+    if (lane == r) {
+      *wak = ak, *wai = ai, *wbk = bk, *wbi = bi;
+    }
+    if (ak != 0u && ka[0] == ak && ia[0] == ai) pop(ka, ia);
+    if (bk != 0u && kb[0] == bk && ib[0] == bi) pop(kb, ib);
+  }
+}
+
 // One warp: the K best of n unsorted entries at ck/ci (K rounds; each
 // round's winner is struck out in place).  Winners go to ok/oi[r].
 __device__ __forceinline__ void warp_select_keys(uint32_t *ck, uint32_t *ci, int n, int K, uint32_t *ok,
                                                  uint32_t *oi) {
   const int lane = threadIdx.x & (kWarp - 1);
+#pragma unroll 1  // code size: these loops run once per call
   for (int r = 0; r < K; ++r) {
     uint32_t lk = 0u, li = (uint32_t)kEmptyId;
     int lq = -1;
@@ -414,5 +449,33 @@ int umma_tiles(int W_max);
 int umma_cluster();
 cudaError_t prepare_umma_kernels();
 cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st);
+
+// One-launch decode step (ns_step.cu): the state update and the fused
+// gather + projection + top-k of one sequence in one cooperative launch.
+constexpr int kMaxStepCtas = 256;  // most CTAs of a step launch (the verify-candidate buffer's rows)
+struct StepLaunch {
+  SeqDev s;
+  Dims d;
+  const uint16_t *W;         // W_head [V x H]
+  const uint16_t *hid;       // [n x H]
+  int32_t n, k;
+  float *logits;             // [n x ld]
+  int32_t ld;
+  int32_t *out_ids;          // [n x k]
+  float *out_vals;
+  uint32_t *err;
+  const int32_t *tree;       // [n_tree]
+  int32_t n_tree;
+  const float *zrow;         // the verify row (null when K_ver = 0)
+  int32_t clusters, tiles_per_cluster, cluster_size;  // from step_plan
+  bool probe;                // launch check: every CTA returns at once
+};
+// Sets the kernel's shared-memory limit and counts its resident clusters.
+cudaError_t prepare_step_kernel();
+// Clusters of a step launch for these dimensions (0: the configuration needs
+// the two-launch path); *tiles_per_cluster gets the tiles each cluster runs,
+// *cluster_size its CTAs.
+int step_plan(const Dims &d, int *tiles_per_cluster, int *cluster_size);
+cudaError_t launch_step(const StepLaunch &L, cudaStream_t st);
 
 }  // namespace ns

@@ -35,9 +35,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait on a phase; false (and NS_FLAG_TIMEOUT) when it runs out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The waiting part of mbar_wait, kept out of line: it is reached only when
+// the phase has not completed at the first test, and inlining it at every
+// wait would multiply the kernels' code (their instruction-cache footprint).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint32_t *err) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > kWaitCycles) {
@@ -46,6 +47,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
     }
   }
   return true;
+}
+// Bounded wait on a phase; false (and NS_FLAG_TIMEOUT) when it runs out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, err);
 }
 
 // Untiled bulk copy global -> this CTA's shared memory, completing on `bar`.

@@ -175,6 +175,7 @@ __global__ void init_reset_kernel(SeqDev s, Dims d) {
     *s.count = 0;
     s.slot_meta[0] = 0;
     s.slot_meta[1] = 0;
+    *s.gbar = 0ull;
   }
 }
 

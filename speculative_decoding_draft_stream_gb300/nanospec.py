@@ -35,6 +35,7 @@ EXPORTED = (
     "ns_dense_lm_head_topk", "ns_get_active", "ns_get_state", "ns_get_error", "ns_state_update",
     "ns_gather_sub_lm_head_topk", "ns_trace_events", "ns_dense_lm_head_topk_noalloc", "ns_gather_new_head_rows",
     "ns_slot_lm_head_logits_topk", "ns_step_slots", "ns_get_slots", "ns_step_batch", "ns_sub_lm_head_indexed_topk",
+    "ns_step_launches",
 )
 NOALLOC_MAX_LOGITS = 1 << 20
 
@@ -67,6 +68,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "ns_create": (I32, [ctypes.POINTER(ns_config), ctypes.POINTER(P)]),
         "ns_destroy": (I32, [P]),
         "ns_device_bytes": (I64, [P]),
+        "ns_step_launches": (I32, [P]),
         "ns_stream_init": (I32, [P, I32, P, I32, P, P]),
         "ns_stream_append": (I32, [P, I32, P, I32, P, I32, I32, P]),
         "ns_build_active_vocab": (I32, [P, I32, P]),
@@ -170,6 +172,11 @@ class Handle:
     @property
     def device_bytes(self) -> int:
         return int(self._lib.ns_device_bytes(self._h))
+
+    @property
+    def step_launches(self) -> int:
+        """Kernel launches of one ns_step on this handle (1: the one-launch step)."""
+        return int(self._lib.ns_step_launches(self._h))
 
     # -- the C ABI -------------------------------------------------------------
     def stream_init(self, seq: int, prompt: Optional[torch.Tensor], prefill_logits: Optional[torch.Tensor],

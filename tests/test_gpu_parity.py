@@ -36,7 +36,12 @@ def _handle(pkg, cfg, batch=1, max_prompt=None, max_k=None):
                       max_k=max_k or cfg.k, batch=batch, max_prompt=max_prompt or 4096)
 
 
-def _run_workload(pkg, cfg: WorkloadConfig, fused: bool, logit_steps=None, seq=0, h=None,
+# How a decode step is issued: the five calls of the problem statement, ns_step
+# (one cooperative launch where the device holds its grid), or its two halves.
+MODES = ["separate_calls", "fused_step", "two_launch"]
+
+
+def _run_workload(pkg, cfg: WorkloadConfig, mode: str, logit_steps=None, seq=0, h=None,
                   W_dev=None, wl=None):
     """Init + every decode step; returns the oracle stream.
 
@@ -65,8 +70,11 @@ def _run_workload(pkg, cfg: WorkloadConfig, fused: bool, logit_steps=None, seq=0
             tree_d = dev_i32(trees[t])
             vb_d = dev_f32(vb) if vb is not None else None
             hid_d = dev_bf16(hid)
-            if fused:
+            if mode == "fused_step":
                 ids, vals = h.step(seq, tree_d, vb_d, vr, W_dev, hid_d, cfg.k, logits=logits)
+            elif mode == "two_launch":
+                h.state_update(seq, tree_d, vb_d, vr)
+                ids, vals = h.gather_sub_lm_head_topk(seq, W_dev, hid_d, cfg.k, logits=logits)
             else:
                 h.stream_append(seq, tree_d, vb_d, vr)
                 h.build_active_vocab(seq)
@@ -89,9 +97,9 @@ def _run_workload(pkg, cfg: WorkloadConfig, fused: bool, logit_steps=None, seq=0
 TOY = get_config("toy_v4096_h256")
 
 
-@pytest.mark.parametrize("fused", [False, True], ids=["separate_calls", "fused_step"])
-def test_toy_every_step(pkg, fused):
-    _run_workload(pkg, TOY, fused)
+@pytest.mark.parametrize("mode", MODES)
+def test_toy_every_step(pkg, mode):
+    _run_workload(pkg, TOY, mode)
 
 
 # A mid-size head: several row tiles, a ragged last tile, H split over a cluster,
@@ -100,9 +108,9 @@ MID = WorkloadConfig(name="mid", V=20011, H=1024, W_max=1000, K_pre=3, K_ver=3, 
                      zipf_s=1.05, steps=12, n_tree=60, tree_local=0.7, tree_recent=256, n_verify=4)
 
 
-@pytest.mark.parametrize("fused", [False, True], ids=["separate_calls", "fused_step"])
-def test_mid_every_step(pkg, fused):
-    _run_workload(pkg, MID, fused)
+@pytest.mark.parametrize("mode", MODES)
+def test_mid_every_step(pkg, mode):
+    _run_workload(pkg, MID, mode)
 
 
 # Full-width heads on a small vocabulary: H = 4096 and 3584 give every CTA of
@@ -117,8 +125,9 @@ WIDE = [
 
 
 @pytest.mark.parametrize("cfg", WIDE, ids=lambda c: c.name)
-def test_wide_heads_every_step(pkg, cfg):
-    _run_workload(pkg, cfg, True)
+@pytest.mark.parametrize("mode", ["fused_step", "two_launch"])
+def test_wide_heads_every_step(pkg, cfg, mode):
+    _run_workload(pkg, cfg, mode)
 
 
 EDGE = [
@@ -144,9 +153,9 @@ EDGE = [
 
 
 @pytest.mark.parametrize("cfg", EDGE, ids=lambda c: c.name)
-@pytest.mark.parametrize("fused", [False, True], ids=["separate_calls", "fused_step"])
-def test_edge_configs(pkg, cfg, fused):
-    _run_workload(pkg, cfg, fused)
+@pytest.mark.parametrize("mode", MODES)
+def test_edge_configs(pkg, cfg, mode):
+    _run_workload(pkg, cfg, mode)
 
 
 def test_empty_tree_and_reinit(pkg):
