@@ -38,7 +38,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // The waiting part of mbar_wait, kept out of line: it is reached only when
 // the phase has not completed at the first test, and inlining it at every
 // wait would multiply the kernels' code (their instruction-cache footprint).
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint32_t *err) {
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint32_t *err) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > kWaitCycles) {
