@@ -312,6 +312,53 @@ __device__ __forceinline__ void warp_topk4_pair(uint32_t *ka, uint32_t *ia, uint
   }
 }
 
+// Sorts eight (key, id) pairs best first (key descending, then id
+// ascending): Batcher's odd-even merge network, 19 compare-exchanges.
+__device__ __forceinline__ void sort8_desc(uint32_t *k, uint32_t *i) {
+  auto cs = [&](int x, int y) {
+    if (k[y] > k[x] || (k[y] == k[x] && i[y] < i[x])) {
+      const uint32_t tk = k[x], ti = i[x];
+      k[x] = k[y];
+      i[x] = i[y];
+      k[y] = tk;
+      i[y] = ti;
+    }
+  };
+  cs(0, 1), cs(2, 3), cs(4, 5), cs(6, 7);
+  cs(0, 2), cs(1, 3), cs(4, 6), cs(5, 7);
+  cs(1, 2), cs(5, 6);
+  cs(0, 4), cs(1, 5), cs(2, 6), cs(3, 7);
+  cs(2, 4), cs(3, 5);
+  cs(1, 2), cs(3, 4), cs(5, 6);
+}
+
+// One warp: the K best of eight (key, id) pairs per lane; lane r ends with
+// winner r (r < K) in *wk/*wi.
+__device__ __forceinline__ void warp_topk8_lanes(uint32_t *hk, uint32_t *hi, int K, uint32_t *wk, uint32_t *wi) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  sort8_desc(hk, hi);
+  *wk = 0u;
+  *wi = (uint32_t)kEmptyId;
+#pragma unroll 1
+  for (int r = 0; r < K; ++r) {
+    uint32_t bk, bi;
+    warp_best(hk[0], hi[0], bk, bi);
+    if (lane == r) {
+      *wk = bk;
+      *wi = bi;
+    }
+    if (bk != 0u && hk[0] == bk && hi[0] == bi) {
+#pragma unroll
+      for (int q = 0; q < 7; ++q) {
+        hk[q] = hk[q + 1];
+        hi[q] = hi[q + 1];
+      }
+      hk[7] = 0u;
+      hi[7] = (uint32_t)kEmptyId;
+    }
+  }
+}
+
 // One warp: the K best of n unsorted entries at ck/ci (K rounds; each
 // round's winner is struck out in place).  Winners go to ok/oi[r].
 __device__ __forceinline__ void warp_select_keys(uint32_t *ck, uint32_t *ci, int n, int K, uint32_t *ok,

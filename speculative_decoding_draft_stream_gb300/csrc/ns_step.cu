@@ -203,14 +203,14 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kUThreads, 1)
   int32_t *s_ring = wbase + L.ring;
   long long *s_len = reinterpret_cast<long long *>(wbase + L.len);
   int32_t *s_goff = wbase + L.goff;
-  uint32_t *s_vk = reinterpret_cast<uint32_t *>(wbase + L.vk);
-  uint32_t *s_vi = reinterpret_cast<uint32_t *>(wbase + L.vi);
   int *h_key = wbase + L.hash, *h_last = h_key + kStepHash, *h_ev = h_last + kStepHash, *h_ap = h_ev + kStepHash;
   uint32_t *s_filt = reinterpret_cast<uint32_t *>(wbase + L.filt);
   uint32_t *wl_k = reinterpret_cast<uint32_t *>(wbase + L.wl), *wl_i = wl_k + (kStepWarps + 1) * NS_MAX_SELECT_K;
   uint32_t *res_k = wl_i + (kStepWarps + 1) * NS_MAX_SELECT_K, *res_i = res_k + NS_MAX_SELECT_K;
   int *s_tree = wbase + L.small, *s_app = s_tree + NS_MAX_ROWS, *s_evid = s_app + kMaxAppendStep;
   int *s_misc = s_evid + kMaxAppendStep, *sh_scan = s_misc + 4;
+  uint32_t *s_vk = reinterpret_cast<uint32_t *>(wbase + L.vk);
+  uint32_t *s_vi = reinterpret_cast<uint32_t *>(wbase + L.vi);
   const uint32_t sbar = smem_u32(&s_sbar);
 
   // ---- phase A: the loads of the old state and of the verify slice ---------
@@ -273,10 +273,6 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kUThreads, 1)
     h_ap[q] = 0;
   }
   for (int q = tid; q < kFilterWords; q += kUThreads) s_filt[q] = 0u;
-  if (tid < K) {
-    wl_k[kStepWarps * K + tid] = 0u;  // the running Top-K starts empty
-    wl_i[kStepWarps * K + tid] = (uint32_t)kEmptyId;
-  }
   if (warp == 1) tmem_alloc(smem_u32(S.tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -366,6 +362,10 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kUThreads, 1)
 
   // the slice's Top-K: per pass, each warp's K best of its lanes' four
   // values, then warp 0 merges the warps' lists with the running result
+  if (tid < K) {
+    wl_k[kStepWarps * K + tid] = 0u;  // the running Top-K starts empty
+    wl_i[kStepWarps * K + tid] = (uint32_t)kEmptyId;
+  }
   for (int c0 = 0; c0 < nsl; c0 += 4 * kUThreads) {
     if (c0 == 4 * kUThreads) {
 #pragma unroll
@@ -533,7 +533,6 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kUThreads, 1)
         if (tid >= sh0 && tid < sh0 + shn) a.active[p] = id;  // this CTA's share of the tile
       }
     }
-    if (m_act == 0 && cid == 0) umma_pad_topk<kCL>(u.out_ids, u.out_vals, u.n, u.k);  // an empty I_t
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the ring area goes back to the tiles
     __syncthreads();
   }
@@ -549,8 +548,66 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kUThreads, 1)
     const int row0 = tile * kUM;
     if (tid < kUM) S.s_rows[tid] = s_tiles[j * kUM + (row0 + tid < m_act ? tid : m_act - 1 - row0)];
     __syncthreads();
-    umma_tile<kCL, false, false>(S, tmem, tmH, tmP, u, iter, nk, tile, 0, m_act, T);
+    umma_tile<kCL, false, false, false>(S, tmem, tmH, tmP, u, iter, nk, tile, 0, m_act, T);
     ++iter;
+  }
+
+  // ---- top-k: every CTA ranks whole rows of the logits the tiles wrote ----
+  // (rows cta, cta + P, ...; 8 columns per thread per pass, ties to the
+  // smaller column, which is the smaller id as I_t ascends)
+  if (ok) ok = grid_barrier(a.gbar, (unsigned long long)P, u.err, &s_misc[3]);
+  if (ok) {
+    uint32_t *rk = reinterpret_cast<uint32_t *>(S.gbase);  // [(warps + 1) x K] lists, then the result
+    uint32_t *ri = rk + (kStepWarps + 1) * NS_MAX_TOPK;
+    uint32_t *ok_k = ri + (kStepWarps + 1) * NS_MAX_TOPK, *ok_i = ok_k + NS_MAX_TOPK;
+    const int k = u.k;
+    const bool vec_l = (u.ld % 4 == 0) && (reinterpret_cast<uintptr_t>(u.logits) % 16 == 0);
+    for (int r = cta; r < u.n; r += P) {
+      const float *row = u.logits + (size_t)r * u.ld;
+      if (tid < k) {
+        rk[kStepWarps * k + tid] = 0u;
+        ri[kStepWarps * k + tid] = (uint32_t)kEmptyId;
+      }
+      for (int c0 = 0; c0 < m_act; c0 += 8 * kUThreads) {
+        uint32_t hk[8], hi[8];
+        const int j0 = c0 + 8 * tid;
+        if (vec_l && j0 + 8 <= m_act) {
+          const float4 f0 = __ldcg(reinterpret_cast<const float4 *>(row + j0));
+          const float4 f1 = __ldcg(reinterpret_cast<const float4 *>(row + j0 + 4));
+          const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+          for (int q = 0; q < 8; ++q) hk[q] = order_key(v[q]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) hk[q] = j0 + q < m_act ? order_key(__ldcg(row + j0 + q)) : 0u;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) hi[q] = hk[q] != 0u ? (uint32_t)(j0 + q) : (uint32_t)kEmptyId;
+        uint32_t wk, wi;
+        warp_topk8_lanes(hk, hi, k, &wk, &wi);
+        if (lane < k) {
+          rk[warp * k + lane] = wk;
+          ri[warp * k + lane] = wi;
+        }
+        __syncthreads();
+        if (warp == 0) {
+          uint32_t lk, li;
+          warp_merge_lists(rk, ri, kStepWarps + 1, k, ok_k, ok_i, lk, li);
+          if (lane < k) {
+            rk[kStepWarps * k + lane] = ok_k[lane];
+            ri[kStepWarps * k + lane] = ok_i[lane];
+          }
+        }
+        __syncthreads();
+      }
+      if (tid < k) {  // column -> id through I_t
+        const uint32_t key = rk[kStepWarps * k + tid];
+        const int j = (int)ri[kStepWarps * k + tid];
+        u.out_ids[r * k + tid] = key != 0u ? __ldcg(a.active + j) : -1;
+        u.out_vals[r * k + tid] = key != 0u ? key_value(key) : -__int_as_float(0x7f800000);
+      }
+      __syncthreads();
+    }
   }
   if (warp == 2 && lane == 0) bulk_wait_all();  // the packed-buffer stores are complete before the CTA leaves
   tc_fence_after();

@@ -257,7 +257,10 @@ __device__ __forceinline__ void umma_init_barriers(const UmmaSmem &S, bool in_pl
 // row0 = tile * kUM; m = rows of the sequence (|I_t|), T = its tiles.  The
 // sequence's candidate lists, ticket, logits and outputs are a's, moved by
 // bseq sequences (kBatch).  Ends with a cluster barrier.
-template <int kUCluster, bool kInPlace, bool kBatch>
+// kTopk: rank each row's tile columns and merge the tiles' lists into the
+// top-k (the last tile of a row slice to finish merges).  Without it the
+// tile only writes its logits, and the caller ranks the rows afterwards.
+template <int kUCluster, bool kInPlace, bool kBatch, bool kTopk = true>
 __device__ __forceinline__ void umma_tile(const UmmaSmem &S, uint32_t tmem, const CUtensorMap &tmH,
                                           const CUtensorMap &tmP, const UmmaArgs &a, int iter, int nk, int tile,
                                           int bseq, int m, int T) {
@@ -406,6 +409,17 @@ __device__ __forceinline__ void umma_tile(const UmmaSmem &S, uint32_t tmem, cons
     *reinterpret_cast<float4 *>(F + rr * kUM + j) = s4;
   }
   __syncthreads();
+
+  if (!kTopk) {  // logits only
+    for (int i = tid; i < nr * kUM; i += kUThreads) {
+      const int rr = i / kUM, j = i % kUM;
+      const int rw = r0 + rr, jg = row0 + j;
+      if (rw < a.n && jg < m) logits[(size_t)rw * a.ld + jg] = F[i];
+    }
+    __syncwarp();
+    cluster_sync();  // peers may still be reading this CTA's partial tile
+    return;
+  }
 
   // ---- per-tile top-k of each row (a warp takes rows w and w + 8) ----------
   // Each lane sorts its four columns (value descending, then id ascending; I_t
