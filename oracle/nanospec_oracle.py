@@ -230,7 +230,7 @@ def topk_remap(logits, I, k: int):
     """Per row, the top-k columns of ``logits`` mapped to global ids through I.
 
     Returns (ids int32 [n, k], vals fp32 [n, k]); rows with fewer than k
-    columns are padded with (-1, -inf).
+    orderable (non-NaN) columns are padded with (-1, -inf).
     """
     logits = np.asarray(logits, dtype=np.float32)
     I = np.asarray(I, dtype=np.int64)
@@ -241,8 +241,9 @@ def topk_remap(logits, I, k: int):
     if kk > 0 and n > 0:
         T = top_k_rows(logits, kk)
         for r in range(n):
-            ids[r, :kk] = I[T[r]]
-            vals[r, :kk] = logits[r, T[r]]
+            t = T[r][T[r] >= 0]
+            ids[r, :len(t)] = I[t]
+            vals[r, :len(t)] = logits[r, t]
     return ids, vals
 
 

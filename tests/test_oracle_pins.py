@@ -301,3 +301,14 @@ def test_topk_remap_pads_short_rows():
     assert vals[0, :2].tolist() == [2.0, 0.5] and np.all(np.isneginf(vals[:, 2:]))
     ids0, vals0 = O.topk_remap(np.zeros((2, 0), np.float32), np.zeros(0, np.int32), 3)
     assert (ids0 == -1).all() and np.isneginf(vals0).all()
+
+
+def test_topk_remap_pads_rows_with_few_orderable_values():
+    # NaN never ranks: a row with fewer than k non-NaN logits ends in (-1, -inf)
+    # padding, whatever its width; infinities rank like any value
+    logits = np.array([[np.nan, 2.0, np.nan, np.inf, np.nan, -np.inf],
+                       [np.nan] * 6], dtype=np.float32)
+    I = np.array([10, 11, 12, 13, 14, 15])
+    ids, vals = O.topk_remap(logits, I, 4)
+    assert ids.tolist() == [[13, 11, 15, -1], [-1, -1, -1, -1]]
+    assert vals[0, :3].tolist() == [np.inf, 2.0, -np.inf] and np.isneginf(vals[0, 3]) and np.all(np.isneginf(vals[1]))
