@@ -5,8 +5,7 @@ One step = one decode step of the hot path on one sequence: verify Top-K,
 draft-tree dedup, stream append, window counts and bitmap, ascending
 compaction into I_t, gather of W_head[I_t, :] into the packed buffer,
 projection of the draft hidden states and top-k remapped to global ids
-(ns_step: two kernels, the state update and the fused tcgen05
-gather + projection + top-k).  Workload: Llama-3-8B-shaped draft head (V=128256,
+(ns_step: one cooperative kernel that does all of it).  Workload: Llama-3-8B-shaped draft head (V=128256,
 H=4096, W_max=3072, K_pre=K_ver=3, 60-node trees, top-10), seeded synthetic
 inputs resident in HBM before the timed region.  L2 (129 MB) is flushed
 before every timed step by writing a 256 MiB buffer, and the time of the
@@ -52,9 +51,11 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-extra", action="store_true", help="skip the dense-head and pinned-point extras")
-    p.add_argument("--sweep", action="store_true",
-                   help="also time the Qwen-2.5-7B-shaped workload and the Qwen3-8B W_max sweep (with its dense "
-                        "heads) into extra.workloads")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip extra.workloads (the Qwen-2.5-7B head, the Qwen3-8B W_max sweep with its dense heads, "
+                        "the 16-sequence batch)")
+    p.add_argument("--workload-steps", type=int, default=24,
+                   help="decode steps per extra workload, from its prefill (0: the workload's full count)")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
     p.add_argument("--decode-steps", type=int, default=0,
                    help="generate inputs for only this many decode steps (0: the workload's count); "
@@ -142,16 +143,18 @@ class ClockSampler:
 
 
 def source_hash() -> str:
+    """Hash of the sources the step kernel is compiled from (the one-launch
+    step and the tcgen05 tile it runs)."""
     h = hashlib.sha256()
-    for f in ("ns_umma.cu", "ns_internal.cuh"):
+    for f in ("ns_step.cu", "ns_umma_tile.cuh", "ns_internal.cuh", "ns_ptx.cuh"):
         with open(os.path.join(ROOT, "speculative_decoding_draft_stream_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic_per_byte():
-    """DRAM bytes per algorithmic byte of the fused gather+projection kernel,
-    from the committed ncu summary, if it was taken on the current source."""
+    """DRAM bytes per algorithmic byte of the step kernel, from the committed
+    ncu summary, if it was taken on the current source."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
@@ -359,19 +362,23 @@ def time_decode(ns, cfg, dev, flush, warmup, inp):
         h.close()
 
 
-def run_sweep(ns, dev, flush, warmup):
+def run_workloads(ns, dev, flush, warmup, steps):
     """The other draft-head shapes: Qwen-2.5-7B (H = 3584) and the Qwen3-8B
-    W_max sweep, each point with its decode steps; the Qwen3 head also with
-    the full-vocabulary dense head (cuBLAS and ours) and the static first-32768
-    sub-head on the same hiddens."""
+    W_max sweep, each point over its first `steps` decode steps from prefill
+    (0: all of them); the Qwen3 head also with the full-vocabulary dense head
+    (cuBLAS and ours) and the static first-32768 sub-head on the same hiddens;
+    the 16-sequence batch."""
     import torch
     from synth import get_config
 
+    def short(cfg):
+        return cfg.with_(steps=min(cfg.steps, steps)) if steps > 0 else cfg
+
     out = {}
-    q25 = get_config("qwen25_7b_v152064_h3584")
+    q25 = short(get_config("qwen25_7b_v152064_h3584"))
     out[q25.name] = time_decode(ns, q25, dev, flush, warmup, decode_inputs(q25, dev))
     torch.cuda.empty_cache()
-    q3 = get_config("qwen3_8b_v151936_h4096")
+    q3 = short(get_config("qwen3_8b_v151936_h4096"))
     inp = decode_inputs(q3, dev)  # the inputs do not depend on W_max
     pts = {}
     for W_max in q3.W_max_sweep:
@@ -396,7 +403,7 @@ def run_sweep(ns, dev, flush, warmup):
     out[q3.name] = {"W_max_sweep": pts, "dense_head": dense}
     del inp, W_d, hid
     torch.cuda.empty_cache()
-    b16 = get_config("batched16_v128256_h4096")
+    b16 = short(get_config("batched16_v128256_h4096"))
     out[b16.name] = time_batched(ns, b16, dev, flush, warmup)
     return out
 
@@ -634,11 +641,21 @@ def run_ours(args):
     m_list = counts.cpu().tolist()
     del g_traced
     pb = sum(proj_bytes(m, n, H) for m in m_list)
-    proj_gbs = pb / (sum(ms_proj) * 1e-3) / 1e9
     sb = sum(step_bytes(m, n, H, V) for m in m_list)
     step_gbs = sb / (total_ms * 1e-3) / 1e9
     peak, peak_kind = load_peaks()
     ratio = ncu_traffic_per_byte()
+    launches = h.step_launches
+    if launches == 1:  # the whole step is one kernel: its bytes are the step's
+        kb, kname = sb, "step_kernel (one-launch decode step: state update, gather, tcgen05 projection, top-k)"
+    else:
+        kb, kname = pb, "umma_step_kernel (fused gather + tcgen05 projection + top-k)"
+    kern_gbs = kb / (sum(ms_proj) * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": kern_gbs, "peak": peak, "unit": "GB/s",
+                "frac": kern_gbs / peak, "peak_kind": f"{peak_kind} hbm_gbs",
+                "traffic": (ratio * kb / K) if ratio is not None else None, "algorithmic_bytes_per_launch": kb / K,
+                "launch_us": 1e3 * float(np.mean(ms_proj)),
+                "timing": "CUDA events around each launch in a traced replay of the same steps"}
 
     # ---- end to end through the public API with host buffers -----------------
     # Each step's inputs (verify logits, draft hiddens, tree ids) sit in one
@@ -671,17 +688,34 @@ def run_ours(args):
     d2h = 2 * n * k * 4
     barrier()
     e2e_s = 0.0
+    # where the time goes: events on the stream around the copies and the
+    # step, host time of the ns_step call itself
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    split = {"h2d_us": 0.0, "step_us": 0.0, "d2h_us": 0.0, "dispatch_us": 0.0}
     for t in range(K):
         u = t % T
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
+        evs[0].record()
         dev_in.copy_(host_in[u], non_blocking=True)
+        evs[1].record()
+        td = time.perf_counter()
         h.step(0, tree_b, ver_b, vrows[u], W_d, hid_b, k, logits=logits, ids=ids_o, vals=vals_o)
+        split["dispatch_us"] += 1e6 * (time.perf_counter() - td)
+        evs[2].record()
         host_out.copy_(dev_out, non_blocking=True)
+        evs[3].record()
         stream.synchronize()
         e2e_s += time.perf_counter() - t0
+        split["h2d_us"] += 1e3 * evs[0].elapsed_time(evs[1])
+        split["step_us"] += 1e3 * evs[1].elapsed_time(evs[2])
+        split["d2h_us"] += 1e3 * evs[2].elapsed_time(evs[3])
     barrier()
+    e2e_split = {key: v / K for key, v in split.items()}
+    e2e_split["wall_us"] = 1e6 * e2e_s / K
+    e2e_split["host_and_sync_us"] = e2e_split["wall_us"] - (e2e_split["h2d_us"] + e2e_split["step_us"] +
+                                                             e2e_split["d2h_us"])
     e2e_s = max_over_ranks(e2e_s)
     e2e = replicas.whole_job_rate(K, world, e2e_s)
 
@@ -819,7 +853,7 @@ def run_ours(args):
         us_ext = policy_us(ext_init, step)
         extra["policies"] = {"ctx_only_step_us": us_ctx, "ext_only_step_us": us_ext,
                              "ctx_plus_ext_step_us": 1e3 * total_ms / K,
-                             "note": "64 steps from the initial state each; the headline averages 512"}
+                             "note": f"64 steps from the initial state each; the headline is the first {K} steps"}
 
         # two-stream pipeline (MicroSpec §3.3): the gather of W_head[I_t, :] on a
         # copy stream while a stand-in draft backbone runs on the compute
@@ -878,8 +912,9 @@ def run_ours(args):
                                "ours_static32768_topk_us": us_static,
                                "speedup_step_vs_cublas_dense": us_cublas / (1e3 * total_ms / K),
                                "speedup_pinned_point_vs_cublas_dense": us_cublas / us0}
-    if args.sweep:
-        extra["workloads"] = run_sweep(ns, dev, flush, args.warmup)
+    if not args.no_extra and not args.no_workloads:
+        torch.cuda.empty_cache()
+        extra["workloads"] = run_workloads(ns, dev, flush, args.warmup, args.workload_steps)
     clock = clocks.stop()
 
     # ---- the CPU oracle on a bounded sample (rank 0, one GPU) ----------------
@@ -904,21 +939,22 @@ def run_ours(args):
                        "timing": "graph of K x (flush + step) minus graph of K x flush, median of 3",
                        "mean_active": mean_m, "min_active": int(min(m_list)), "max_active": int(max(m_list)),
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "umma_step_kernel (fused gather + tcgen05 projection + top-k)",
-                         "achieved": proj_gbs, "peak": peak, "unit": "GB/s", "frac": proj_gbs / peak,
-                         "peak_kind": f"{peak_kind} hbm_gbs",
-                         "traffic": (ratio * pb / K) if ratio is not None else None,
-                         "algorithmic_bytes_per_launch": pb / K},
+            "roofline": roofline,
             "step_roofline": {"achieved": step_gbs, "frac": step_gbs / peak,
                               "bytes_per_step": sb / K},
-            "kernel_us": {"state_update": 1e3 * float(np.mean(ms_state)),
-                          "gather_project_topk": 1e3 * float(np.mean(ms_proj)),
-                          "trace_gap": 1e3 * float(np.mean(ms_topk)),
-                          "traced_step": 1e3 * float(np.mean(ms_traced)),
-                          "timing": "traced replay: events around each kernel, no programmatic overlap"},
+            "kernel_us": ({"step_kernel": 1e3 * float(np.mean(ms_proj)),
+                           "traced_step": 1e3 * float(np.mean(ms_traced)),
+                           "timing": "traced replay: events around the one step kernel"} if launches == 1 else
+                          {"state_update": 1e3 * float(np.mean(ms_state)),
+                           "gather_project_topk": 1e3 * float(np.mean(ms_proj)),
+                           "trace_gap": 1e3 * float(np.mean(ms_topk)),
+                           "traced_step": 1e3 * float(np.mean(ms_traced)),
+                           "timing": "traced replay: events around each kernel, no programmatic overlap"}),
+            "step_launches": launches,
             "init_ms": init_ms,
-            "e2e": {"value": e2e, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 2 * K,
+            "e2e": {"value": e2e, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "split_us_per_step": e2e_split},
+            "gpu_launches": launches * K,
             "clocks": clock,
             "cpu_baseline": cpu,
             "extra": extra,

@@ -337,9 +337,13 @@ NS_API ns_status ns_dense_lm_head_topk(ns_handle *h, const uint16_t *d_W_head, i
  * instead of through a handle: logits over rows [0, rows) of W_head (bf16
  * [rows x H], 64 <= H <= 8192, H % 64 == 0) and per-row top-k with ids = row
  * numbers.  It calls no cudaMalloc/cudaFree and no allocating library
- * routine.  Its scratch is a fixed array of about 6.6 MB inside the library
- * image, reserved on every GPU that loads the library until the process
- * exits.  When d_logits is NULL the logits are kept in that scratch, which
+ * routine.  Its scratch is a fixed array of 6,817,792 bytes (6.5 MiB) inside
+ * the library image, reserved on every GPU that loads the library until the
+ * process exits.  It runs one CTA per SM where ns_dense_lm_head_topk runs
+ * two, so it is slower on large heads, and it splits the sum over H
+ * differently: the logits agree with the handle's to fp32 rounding, not bit
+ * for bit.  `stream` must belong to the current device (NS_ERR_ARG
+ * otherwise).  When d_logits is NULL the logits are kept in that scratch, which
  * holds at most NS_NOALLOC_MAX_LOGITS values: n * rows above that returns
  * NS_ERR_ARG (pass d_logits for larger heads, e.g. the full vocabulary).
  * The first call on each device looks up the scratch's device address and

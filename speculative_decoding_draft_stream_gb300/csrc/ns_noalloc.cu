@@ -15,7 +15,7 @@
 
 namespace {
 
-// Scratch layout (floats, 256-byte aligned pieces):
+// Scratch layout (floats, 256-byte aligned pieces; 6,817,792 bytes in all):
 //   [0, kTicketWords)                 per-tile arrival counters (int32)
 //   [kPartOff, kPartOff + kPartFloats) split-K partial tiles
 //   [kLogitsOff, + NS_NOALLOC_MAX_LOGITS) logits when the caller passes none
@@ -64,6 +64,9 @@ cudaError_t setup_current_device(DeviceSetup **out) {
     e = ns::prepare_project_kernels();
     if (e != cudaSuccess) return e;
     s.scratch = static_cast<float *>(ptr);
+    // one CTA per SM (at most kSlots): the handle's dense head runs two per
+    // SM, so this one is slower on large heads and splits K differently
+    // (the same logits up to fp32 summation order)
     s.grid = sms < kSlots ? sms : kSlots;
     s.ready = true;
   }
@@ -89,6 +92,11 @@ extern "C" ns_status ns_dense_lm_head_topk_noalloc(const uint16_t *d_W_head, int
   DeviceSetup *s = nullptr;
   if (setup_current_device(&s) != cudaSuccess) return NS_ERR_CUDA;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // The scratch address is the current device's copy: a stream of another
+  // device would run the kernels against the wrong GPU's array.
+  int cur = 0, sdev = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess || cudaStreamGetDevice(cs, &sdev) != cudaSuccess) return NS_ERR_CUDA;
+  if (sdev != cur) return NS_ERR_ARG;
   float *base = s->scratch;
   int32_t *tickets = reinterpret_cast<int32_t *>(base);
   // The arrival counters must start at zero; everything else is written

@@ -34,7 +34,7 @@ def _sampled(steps):
     return set(range(min(4, steps))) | set(range(0, steps, 16)) | {steps - 1}
 
 
-def _run(pkg, cfg, wl, W, W_dev, h, seq, max_steps=None):
+def _run(pkg, cfg, wl, W, W_dev, h, seq, max_steps=None, mode="step"):
     steps = cfg.steps if max_steps is None else min(cfg.steps, max_steps)
     sample = _sampled(steps)
     prompt = wl.prompt(seq)
@@ -50,7 +50,13 @@ def _run(pkg, cfg, wl, W, W_dev, h, seq, max_steps=None):
     sizes = []
     for t in range(steps):
         vb, vr, hid = wl.verify_logits(seq, t), wl.verify_row(seq, t), wl.hiddens(seq, t)
-        ids, vals = h.step(seq, dev_i32(trees[t]), dev_f32(vb), vr, W_dev, dev_bf16(hid), cfg.k, logits=logits)
+        if mode == "step":
+            ids, vals = h.step(seq, dev_i32(trees[t]), dev_f32(vb), vr, W_dev, dev_bf16(hid), cfg.k, logits=logits)
+        else:  # the five calls of the problem statement, as a caller would issue them
+            h.stream_append(seq, dev_i32(trees[t]), dev_f32(vb), vr)
+            h.build_active_vocab(seq)
+            h.gather_head_rows(seq, W_dev)
+            ids, vals = h.sub_lm_head_logits_topk(seq, dev_bf16(hid), cfg.k, logits=logits)
         ost.append(trees[t], vb, vr)
         I = check_state(h, seq, ost, full=t in sample)
         sizes.append(len(I))
@@ -69,6 +75,21 @@ def test_full_config(pkg, name):
     with pkg.Handle(cfg.V, cfg.H, cfg.W_max, cfg.K_pre, cfg.K_ver, max_tree=cfg.n_tree, max_k=cfg.k,
                     max_prompt=cfg.prompt_len) as h:
         sizes = _run(pkg, cfg, wl, W, W_dev, h, 0)
+        assert h.get_error() == 0
+    assert max(sizes) <= cfg.W_max and min(sizes) > 0
+
+
+def test_full_config_separate_calls(pkg):
+    """The Llama-3-shaped head through ns_stream_append, ns_build_active_vocab,
+    ns_gather_head_rows and ns_sub_lm_head_logits_topk (the pages' two-stream
+    calls, here on one stream), on its first 24 steps."""
+    cfg = get_config("llama3_8b_v128256_h4096")
+    wl = Workload(cfg)
+    W = wl.w_head()
+    W_dev = dev_bf16(W)
+    with pkg.Handle(cfg.V, cfg.H, cfg.W_max, cfg.K_pre, cfg.K_ver, max_tree=cfg.n_tree, max_k=cfg.k,
+                    max_prompt=cfg.prompt_len) as h:
+        sizes = _run(pkg, cfg, wl, W, W_dev, h, 0, max_steps=24, mode="separate")
         assert h.get_error() == 0
     assert max(sizes) <= cfg.W_max and min(sizes) > 0
 
