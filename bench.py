@@ -441,6 +441,13 @@ def time_batched(ns, cfg, dev, flush, warmup):
         def batched(t):
             h.step_batch(trees_d[t], verify_d[t], vrows[t], W_d, hid_d[t], k, logits=logits, ids=ids, vals=vals)
 
+        u_ids, u_cnt, _, _, cap = h.get_union()
+        u_logits = torch.empty((B, n, cap), dtype=torch.float32, device=dev)
+
+        def unioned(t):
+            h.step_batch_union(trees_d[t], verify_d[t], vrows[t], W_d, hid_d[t], k, logits=u_logits, ids=ids,
+                               vals=vals)
+
         def one_by_one(t):
             for b in range(B):
                 h.step(b, trees_d[t, b], verify_d[t, b], vrows[t][b], W_d, hid_d[t, b], k, logits=logits[b],
@@ -476,7 +483,16 @@ def time_batched(ns, cfg, dev, flush, warmup):
             return 1e3 * sorted(diffs)[1] / T
 
         us_b = per_step_us(batched)
+        us_u = per_step_us(unioned)
         us_s = per_step_us(one_by_one)
+        init()
+        u_rows = torch.zeros(T, dtype=torch.int32, device=dev)
+        sum_rows = torch.zeros(T, dtype=torch.int64, device=dev)
+        for t in range(T):
+            unioned(t)
+            u_rows[t:t + 1].copy_(u_cnt)
+            sum_rows[t] = sum(h.get_active(b)[1][0].to(torch.int64) for b in range(B))
+        u_rows, sum_rows = u_rows.cpu().numpy(), sum_rows.cpu().numpy()
         init()
         _, cnt, _, _ = h.get_active(0)
         act = torch.zeros((T, B), dtype=torch.int32, device=dev)
@@ -489,7 +505,11 @@ def time_batched(ns, cfg, dev, flush, warmup):
             raise RuntimeError("device error flags set during the batched steps")
         return {"sequences": B, "steps": T, "batched_step_us": us_b, "sequence_steps_per_s": B * 1e6 / us_b,
                 "one_call_per_sequence_step_us": us_s, "speedup_batched": us_s / us_b,
-                "mean_active": float(act.mean())}
+                "mean_active": float(act.mean()),
+                "union_step_us": us_u, "union_sequence_steps_per_s": B * 1e6 / us_u,
+                "union_rows_mean": float(u_rows.mean()), "rows_of_all_sequences_mean": float(sum_rows.mean()),
+                "union_note": "ns_step_batch_union: one gather of W_head[U, :] for the union U of the sequences' "
+                              "I_t; each sequence projects all of U and ranks its own columns"}
     finally:
         h.close()
 

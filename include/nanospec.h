@@ -224,6 +224,43 @@ NS_API ns_status ns_step_batch(ns_handle *h, int32_t n_seq, const int32_t *d_tre
                                ns_stream stream);
 
 /*
+ * One decode step for sequences 0 .. n_seq-1 with ONE gather for all of them
+ * (the batched reading of MicroSpec §3.3's gathering into a contiguous
+ * buffer; the pages serve one sequence): every sequence's state update as in
+ * ns_step_batch, then U = the union of their active vocabularies in
+ * ascending id order (an OR of their window bitmaps, compacted), one gather
+ * of W_head[U, :] into the handle's union buffer, and every sequence's
+ * hidden rows projected through all of U, each sequence ranking only the
+ * columns of its own I_t (its window bitmap is the mask).  A row of W_head
+ * that several sequences hold crosses HBM once.  Results:
+ *   d_logits    fp32 [n_seq x n x ld_logits] or NULL, ld_logits >= the union
+ *               capacity (ns_get_union): sequence b's logits over all of U,
+ *               column j <-> U[j], columns >= |U| untouched
+ *   d_topk_ids/vals  [n_seq x n x k]: as ns_step_batch (each sequence's top-k
+ *               over its own I_t; equal to ns_step_batch's up to rounding)
+ * Other arguments as ns_step_batch.  The handle must hold more than one
+ * sequence (NS_ERR_STATE otherwise: it has no union buffers).
+ */
+NS_API ns_status ns_step_batch_union(ns_handle *h, int32_t n_seq, const int32_t *d_tree_ids, int32_t n_tree,
+                                     const float *d_verify_logits, int32_t n_verify, const int32_t *verify_rows,
+                                     const uint16_t *d_W_head, const uint16_t *d_hidden, int32_t n, int32_t k,
+                                     float *d_logits, int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
+                                     ns_stream stream);
+
+/*
+ * Device pointers to the union of the last ns_step_batch_union (owned by the
+ * handle; NS_ERR_STATE for a handle of one sequence).  Any out-pointer may be
+ * NULL.
+ *   ids       int32 [capacity]   U ascending (first *count valid)
+ *   count     int32 [1]          |U|
+ *   bitmap    uint32 [ceil(V/32)] bit i set iff i in U
+ *   packed    bf16 [capacity x H] rows j < |U| = W_head[U[j], :]
+ *   capacity  HOST int64: min(batch x W_max, V)
+ */
+NS_API ns_status ns_get_union(ns_handle *h, const int32_t **ids, const int32_t **count, const uint32_t **bitmap,
+                              const uint16_t **packed, int64_t *capacity);
+
+/*
  * The state half of ns_step in one launch: ns_stream_append followed by
  * ns_build_active_vocab (the "GPU-resident state update" that determines
  * I_{t+1}, MicroSpec §3.3).  Arguments as ns_stream_append.

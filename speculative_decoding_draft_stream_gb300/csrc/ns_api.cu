@@ -32,6 +32,18 @@ struct ns_handle {
   int step_clusters = 0;  // clusters of the one-launch step (0: two launches)
   int step_tpc = 0;       // tiles per cluster of the one-launch step
   int step_cl = 0;        // CTAs per cluster of the one-launch step
+  // union of the sequences' active vocabularies (batch > 1): its bitmap, ids
+  // and count, the packed rows W_head[U, :], logits scratch and, per
+  // sequence, candidate lists and tickets of the union projection
+  long long u_cap = 0;  // most union rows: min(batch * W_max, V)
+  int u_ld = 0;
+  uint32_t *u_bitmap = nullptr;
+  int32_t *u_ids = nullptr, *u_count = nullptr;
+  uint16_t *u_packed = nullptr;
+  float *u_logits = nullptr;
+  uint32_t *u_cand = nullptr;
+  long long u_cand_words = 0;   // one candidate array of one sequence
+  long long u_block_words = 0;  // one sequence's block: keys, ids, tickets
   cudaEvent_t trace[4] = {nullptr, nullptr, nullptr, nullptr};
   bool tracing = false;
   long long seq_bytes = 0;  // distance between consecutive sequences' state
@@ -89,6 +101,19 @@ void layout(ns_handle *h, Carver &cv) {
     s.gbar = cv.take<unsigned long long>(1);
     s.vcand_k = cv.take<uint32_t>((size_t)ns::kMaxStepCtas * (c.K_ver > 0 ? c.K_ver : 1));
     s.vcand_i = cv.take<uint32_t>((size_t)ns::kMaxStepCtas * (c.K_ver > 0 ? c.K_ver : 1));
+  }
+  if (c.batch > 1) {
+    const long long cap = (long long)c.batch * c.W_max;
+    h->u_cap = cap < c.V ? cap : c.V;
+    h->u_ld = (int)((h->u_cap + 3) & ~3LL);
+    h->u_bitmap = cv.take<uint32_t>(d.nwords_pad);
+    h->u_ids = cv.take<int32_t>((size_t)h->u_cap);
+    h->u_count = cv.take<int32_t>(1);
+    h->u_packed = cv.take<uint16_t>((size_t)h->u_cap * c.H);
+    h->u_logits = cv.take<float>((size_t)c.batch * ns::kProjBN * h->u_ld);
+    h->u_cand_words = (long long)ns::umma_tiles((int)h->u_cap) * ns::kProjBN * c.max_k;
+    h->u_block_words = ((2 * h->u_cand_words + ns::umma_cluster()) + 63) & ~63LL;
+    h->u_cand = cv.take<uint32_t>((size_t)c.batch * h->u_block_words);
   }
   h->dense_ld = (c.V + 3) & ~3;
   h->dense_logits = cv.take<float>((size_t)ns::kProjBN * h->dense_ld);
@@ -508,6 +533,99 @@ ns_status ns_step_batch(ns_handle *h, int32_t n_seq, const int32_t *d_tree_ids, 
     e = ns::launch_umma_step(L, cs);
   }
   return cuda_status(e);
+}
+
+ns_status ns_step_batch_union(ns_handle *h, int32_t n_seq, const int32_t *d_tree_ids, int32_t n_tree,
+                              const float *d_verify_logits, int32_t n_verify, const int32_t *verify_rows,
+                              const uint16_t *d_W_head, const uint16_t *d_hidden, int32_t n, int32_t k,
+                              float *d_logits, int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
+                              ns_stream stream) {
+  if (!h || n_seq < 1 || n_seq > h->cfg.batch) return NS_ERR_ARG;
+  if (h->u_cap == 0) return NS_ERR_STATE;  // a handle of one sequence has no union buffers
+  if (n_tree < 0 || n_tree > h->cfg.max_tree || (n_tree > 0 && !d_tree_ids)) return NS_ERR_ARG;
+  const int V = h->cfg.V, H = h->cfg.H;
+  if (h->cfg.K_ver > 0) {
+    if (!d_verify_logits || n_verify < 1 || !verify_rows) return NS_ERR_ARG;
+    for (int b = 0; b < n_seq; ++b)
+      if (verify_rows[b] < 0 || verify_rows[b] >= n_verify) return NS_ERR_ARG;
+  }
+  if (!d_W_head || !aligned16(d_W_head)) return NS_ERR_ARG;
+  ns_status st = check_proj_args(h, d_hidden, n, k, d_logits, ld_logits, (int32_t)h->u_cap, d_topk_ids, d_topk_vals);
+  if (st != NS_OK) return st;
+  for (int b = 0; b < n_seq; ++b)
+    if (!h->inited[b]) return NS_ERR_STATE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  // 1. every sequence's state update and its own I_t
+  for (int c0 = 0; c0 < n_seq && e == cudaSuccess; c0 += ns::kMaxBatchLaunch) {
+    const int nb = n_seq - c0 < ns::kMaxBatchLaunch ? n_seq - c0 : ns::kMaxBatchLaunch;
+    ns::StepBatch bt{};
+    bt.seq_bytes = h->seq_bytes;
+    bt.tree_stride = n_tree;
+    bt.z_stride = (long long)n_verify * V;
+    const float *verify = nullptr;
+    if (h->cfg.K_ver > 0) {
+      verify = d_verify_logits + (size_t)c0 * n_verify * V;
+      for (int b = 0; b < nb; ++b) bt.vrow[b] = verify_rows[c0 + b];
+    }
+    e = ns::launch_append_batch(h->seqs[c0], h->dims, nb, n_tree > 0 ? d_tree_ids + (size_t)c0 * n_tree : d_tree_ids,
+                                n_tree, verify, bt, h->err, cs);
+  }
+  // 2. U = the union of their windows, ascending; 3. one gather of W_head[U, :]
+  ns::SeqDev u{};
+  u.bitmap = h->u_bitmap;
+  u.active = h->u_ids;
+  u.count = h->u_count;
+  u.packed = h->u_packed;
+  ns::Dims du = h->dims;
+  du.W_max = (int32_t)h->u_cap;
+  if (e == cudaSuccess) e = ns::launch_union_bitmap(h->seqs[0], h->dims, n_seq, h->seq_bytes, h->u_bitmap, cs);
+  if (e == cudaSuccess) e = ns::launch_build(u, du, h->err, cs);
+  if (e == cudaSuccess) e = ns::launch_gather(u, du, d_W_head, h->ggrid, cs);
+  // 4. every sequence's hidden rows through the union rows, each ranking its own
+  for (int c0 = 0; c0 < n_seq && e == cudaSuccess; c0 += ns::kMaxBatchLaunch) {
+    const int nb = n_seq - c0 < ns::kMaxBatchLaunch ? n_seq - c0 : ns::kMaxBatchLaunch;
+    ns::UmmaLaunch L{};
+    L.W = h->u_packed;
+    L.V = V;
+    L.H = H;
+    L.hid = d_hidden + (size_t)c0 * n * H;
+    L.n = n;
+    L.packed = h->u_packed;
+    L.W_max = (int32_t)h->u_cap;
+    L.idx = h->u_ids;
+    L.count_ptr = h->u_count;
+    L.k = k;
+    L.logits = d_logits ? d_logits + (size_t)c0 * n * ld_logits : h->u_logits + (size_t)c0 * ns::kProjBN * h->u_ld;
+    L.ld = d_logits ? ld_logits : h->u_ld;
+    uint32_t *blk = h->u_cand + (size_t)c0 * h->u_block_words;
+    L.cand_k = blk;
+    L.cand_i = blk + h->u_cand_words;
+    L.slice_ticket = reinterpret_cast<int32_t *>(blk + 2 * h->u_cand_words);
+    L.cand_stride = h->u_block_words * 4;
+    L.out_ids = d_topk_ids + (size_t)c0 * n * k;
+    L.out_vals = d_topk_vals + (size_t)c0 * n * k;
+    L.err = h->err;
+    L.in_place = true;
+    L.nseq = nb;
+    L.seq_bytes = h->seq_bytes;
+    L.logits_bytes = d_logits ? (long long)n * ld_logits * 4 : (long long)ns::kProjBN * h->u_ld * 4;
+    L.mask = h->seqs[c0].bitmap;
+    e = ns::launch_umma_step(L, cs);
+  }
+  return cuda_status(e);
+}
+
+ns_status ns_get_union(ns_handle *h, const int32_t **ids, const int32_t **count, const uint32_t **bitmap,
+                       const uint16_t **packed, int64_t *capacity) {
+  if (!h) return NS_ERR_ARG;
+  if (h->u_cap == 0) return NS_ERR_STATE;
+  if (ids) *ids = h->u_ids;
+  if (count) *count = h->u_count;
+  if (bitmap) *bitmap = h->u_bitmap;
+  if (packed) *packed = h->u_packed;
+  if (capacity) *capacity = h->u_cap;
+  return NS_OK;
 }
 
 ns_status ns_trace_events(ns_handle *h, ns_event *events, int32_t n_events) {

@@ -437,6 +437,10 @@ cudaError_t launch_append_batch(const SeqDev &s, const Dims &d, int nseq, const 
 // Sets the state kernels' shared-memory limits and picks d->state_cluster.
 cudaError_t prepare_state_kernels(Dims *d);
 cudaError_t launch_build(const SeqDev &s, const Dims &d, uint32_t *err, cudaStream_t st);
+// out[w] = OR over sequences b < nseq of sequence b's bitmap word w (sequence
+// b's state is b * seq_bytes past s's).
+cudaError_t launch_union_bitmap(const SeqDev &s, const Dims &d, int nseq, long long seq_bytes, uint32_t *out,
+                                cudaStream_t st);
 cudaError_t launch_gather(const SeqDev &s, const Dims &d, const uint16_t *W, int grid, cudaStream_t st);
 
 // Slot-stable buffer (ns_slots.cu): update the slot table to I_t, then copy
@@ -491,6 +495,11 @@ struct UmmaLaunch {
   int32_t nseq;
   long long seq_bytes, logits_bytes;
   bool rows_by_id;           // in_place over W_head itself: row j = W row idx[j]
+  // union mode (in_place with nseq sequences): idx/count are one list shared
+  // by all; mask is sequence 0's window bitmap (moved by seq_bytes); the
+  // candidate lists and tickets move by cand_stride (0: seq_bytes)
+  const uint32_t *mask;
+  long long cand_stride;
 };
 int umma_tiles(int W_max);
 int umma_cluster();

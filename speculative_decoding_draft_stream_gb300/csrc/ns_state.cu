@@ -697,6 +697,17 @@ __global__ void __launch_bounds__(kStateThreads) build_kernel(SeqDev s, Dims d, 
   compact_bitmap(s_bits, d.nwords, d.nwords_pad, s_nzw, s_nzo, s.active, s.count, d.W_max, err, sh_scan);
 }
 
+// The union of several sequences' windows: word w of every bitmap ORed.
+__global__ void union_bitmap_kernel(const uint32_t *bitmap0, int nwords_pad, int nseq, long long seq_bytes,
+                                    uint32_t *out) {
+  for (int w = blockIdx.x * blockDim.x + threadIdx.x; w < nwords_pad; w += gridDim.x * blockDim.x) {
+    uint32_t v = 0u;
+    for (int b = 0; b < nseq; ++b)
+      v |= __ldg(reinterpret_cast<const uint32_t *>(reinterpret_cast<const char *>(bitmap0) + b * seq_bytes) + w);
+    out[w] = v;
+  }
+}
+
 // packed[j, :] = W[I_t[j], :]; each CTA copies 4 rows per iteration with all
 // 16-byte loads of those rows issued before the stores.
 constexpr int kGatherThreads = 256;
@@ -866,6 +877,13 @@ cudaError_t launch_append_batch(const SeqDev &s, const Dims &d, int nseq, const 
 
 cudaError_t launch_build(const SeqDev &s, const Dims &d, uint32_t *err, cudaStream_t st) {
   build_kernel<<<1, kStateThreads, (size_t)state_smem_words(d.nwords_pad) * 4, st>>>(s, d, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_union_bitmap(const SeqDev &s, const Dims &d, int nseq, long long seq_bytes, uint32_t *out,
+                                cudaStream_t st) {
+  const int blocks = (d.nwords_pad + 255) / 256;
+  union_bitmap_kernel<<<blocks, 256, 0, st>>>(s.bitmap, d.nwords_pad, nseq, seq_bytes, out);
   return cudaGetLastError();
 }
 

@@ -26,7 +26,9 @@ namespace {
 //
 // kBatch: one launch for several sequences (the hidden and packed tensor maps
 // get a third, per-sequence dimension); the clusters loop over the work items
-// (a tile of a sequence), see below.
+// (a tile of a sequence), see below.  kBatch with kInPlace: every sequence
+// projects the same buffer (the union of the sequences' active rows), and
+// ranks only the rows its own window holds (a.mask).
 template <int kUCluster, bool kInPlace, bool kBatch = false>
 __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1)
     umma_step_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmP,
@@ -63,10 +65,10 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
   int id_first = 0, m0 = 0, T0 = 0;
   if (kBatch) {
     const int t0 = cid / a.nseq, b0 = cid % a.nseq;
-    const int32_t *idx0 = reinterpret_cast<const int32_t *>(reinterpret_cast<const char *>(a.idx) + b0 * a.seq_bytes);
+    const int32_t *idx0 = reinterpret_cast<const int32_t *>(reinterpret_cast<const char *>(a.idx) + b0 * a.idx_stride);
     if (tid < kUM && t0 * kUM + tid < a.W_max) id_first = idx0[t0 * kUM + tid];
     if (tid < a.nseq)
-      s_cnt[tid] = *reinterpret_cast<const int32_t *>(reinterpret_cast<const char *>(a.count_ptr) + tid * a.seq_bytes);
+      s_cnt[tid] = *reinterpret_cast<const int32_t *>(reinterpret_cast<const char *>(a.count_ptr) + tid * a.idx_stride);
     __syncthreads();
   } else {
     if (tid < kUM && cid * kUM + tid < a.W_max) id_first = a.idx[cid * kUM + tid];
@@ -101,8 +103,10 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
     if (tile >= T) break;
   }
   // this sequence's state and outputs
-  const long long so = bseq * a.seq_bytes;
-  const int32_t *idx = reinterpret_cast<const int32_t *>(reinterpret_cast<const char *>(a.idx) + so);
+  const int32_t *idx = reinterpret_cast<const int32_t *>(reinterpret_cast<const char *>(a.idx) + bseq * a.idx_stride);
+  const uint32_t *mask =
+      a.mask ? reinterpret_cast<const uint32_t *>(reinterpret_cast<const char *>(a.mask) + bseq * a.mask_stride)
+             : nullptr;
   int32_t *out_ids = a.out_ids + (long long)bseq * a.n * a.k;
   float *out_vals = a.out_vals + (long long)bseq * a.n * a.k;
   if (kBatch && tile >= T) {  // uniform across the cluster
@@ -119,6 +123,7 @@ __global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(kUThreads, 1
           atomicOr(a.err, NS_FLAG_INTERNAL | (3u << 8));
           id = -1;
         }
+        if (mask && id >= 0 && !((mask[id >> 5] >> (id & 31)) & 1u)) id = -1;  // not this sequence's
         s_ids[tid] = id;
         s_rows[tid] = a.rows_by_id ? (id < 0 ? 0 : id) : j;  // rows_by_id: W_head rows, no packed copy
       } else {
@@ -205,6 +210,7 @@ int umma_cluster() { return 16; }  // the most row slices a launch can use
 
 template <int CL, bool IN_PLACE, bool BATCH>
 cudaError_t allow_umma() {
+  static_assert(CL <= 16, "cluster size");
   cudaError_t e = cudaFuncSetAttribute(umma_step_kernel<CL, IN_PLACE, BATCH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
   if (e == cudaSuccess && CL > 8)
@@ -216,7 +222,7 @@ cudaError_t allow_umma() {
 template <int CL>
 int max_clusters() {
   if (allow_umma<CL, false, false>() != cudaSuccess || allow_umma<CL, true, false>() != cudaSuccess ||
-      allow_umma<CL, false, true>() != cudaSuccess) {
+      allow_umma<CL, false, true>() != cudaSuccess || allow_umma<CL, true, true>() != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -243,6 +249,7 @@ template <int CL>
 cudaError_t launch_cl(cudaLaunchConfig_t &cfg, bool in_place, bool batch, const CUtensorMap &tmH,
                       const CUtensorMap &tmP, const UmmaArgs &a) {
   cfg.gridDim = dim3(cfg.gridDim.x * CL);
+  if (batch && in_place) return cudaLaunchKernelEx(&cfg, umma_step_kernel<CL, true, true>, tmH, tmP, a);
   if (batch) return cudaLaunchKernelEx(&cfg, umma_step_kernel<CL, false, true>, tmH, tmP, a);
   if (in_place) return cudaLaunchKernelEx(&cfg, umma_step_kernel<CL, true, false>, tmH, tmP, a);
   return cudaLaunchKernelEx(&cfg, umma_step_kernel<CL, false, false>, tmH, tmP, a);
@@ -276,12 +283,14 @@ int pick_cluster_size(int items, int *clusters) {
 }
 
 cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
-  const bool batch = L.nseq > 1;
-  if (L.in_place && batch) return cudaErrorInvalidValue;
+  const bool batch = L.nseq > 1 || L.mask != nullptr;
+  if (L.in_place && batch && L.mask == nullptr) return cudaErrorInvalidValue;  // only the union mode
   CUtensorMap tmH, tmP;
+  // in place, nothing is stored: the packed map only needs to be valid
   const bool maps =
       batch ? encode_bf16_3d(&tmH, L.hid, L.H, L.n, L.nseq, (uint64_t)L.n * L.H * 2, kUK, kUN) &&
-                  encode_bf16_3d(&tmP, L.packed, L.H, L.W_max, L.nseq, (uint64_t)L.seq_bytes, kUK, kUM)
+                  (L.in_place ? encode_bf16_2d(&tmP, L.packed, L.H, L.W_max, kUK, kUM)
+                              : encode_bf16_3d(&tmP, L.packed, L.H, L.W_max, L.nseq, (uint64_t)L.seq_bytes, kUK, kUM))
             : encode_bf16_2d(&tmH, L.hid, L.H, L.n, kUK, kUN) && encode_bf16_2d(&tmP, L.packed, L.H, L.W_max, kUK, kUM);
   if (!maps) return cudaErrorInvalidValue;
   UmmaArgs a{};
@@ -303,6 +312,10 @@ cudaError_t launch_umma_step(const UmmaLaunch &L, cudaStream_t st) {
   a.err = L.err;
   const int nseq = batch ? L.nseq : 1;
   a.seq_bytes = L.seq_bytes;
+  a.idx_stride = L.mask ? 0 : L.seq_bytes;  // the union mode: one row-id list for every sequence
+  a.cand_stride = L.cand_stride ? L.cand_stride : L.seq_bytes;
+  a.mask = L.mask;
+  a.mask_stride = L.seq_bytes;
   a.logits_bytes = L.logits_bytes;
   a.nseq = nseq;
   a.tiles_per_seq = umma_tiles(L.W_max);

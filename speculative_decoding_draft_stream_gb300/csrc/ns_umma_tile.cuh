@@ -192,6 +192,12 @@ struct UmmaArgs {
   // entries past
   long long seq_bytes, logits_bytes;
   int32_t nseq, tiles_per_seq;
+  // batch strides in bytes: the row ids and their count (0 when the
+  // sequences share one list) and the candidate lists and tickets; mask
+  // (nullable): sequence 0's window bitmap, moved by mask_stride -- a row
+  // whose id is outside a sequence's window is computed but not ranked for it
+  long long idx_stride, cand_stride, mask_stride;
+  const uint32_t *mask;
   int32_t rows_by_id;  // kInPlace: row j is W row idx[j] (an indexed product, nothing packed)
 };
 
@@ -273,7 +279,7 @@ __device__ __forceinline__ void umma_tile(const UmmaSmem &S, uint32_t tmem, cons
   const uint32_t base = S.base, bar_full = S.bar_full, bar_empty = S.bar_empty, bar_acc = S.bar_acc;
   uint8_t *gbase = S.gbase;
   int *s_rows = S.s_rows, *s_ids = S.s_ids, *s_flag = S.s_flag;
-  const long long so = bseq * a.seq_bytes;
+  const long long so = bseq * a.cand_stride;
   uint32_t *cand_k = reinterpret_cast<uint32_t *>(reinterpret_cast<char *>(a.cand_k) + so);
   uint32_t *cand_i = reinterpret_cast<uint32_t *>(reinterpret_cast<char *>(a.cand_i) + so);
   int32_t *ticket = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(a.slice_ticket) + so);

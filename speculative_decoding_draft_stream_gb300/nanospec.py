@@ -35,7 +35,7 @@ EXPORTED = (
     "ns_dense_lm_head_topk", "ns_get_active", "ns_get_state", "ns_get_error", "ns_state_update",
     "ns_gather_sub_lm_head_topk", "ns_trace_events", "ns_dense_lm_head_topk_noalloc", "ns_gather_new_head_rows",
     "ns_slot_lm_head_logits_topk", "ns_step_slots", "ns_get_slots", "ns_step_batch", "ns_sub_lm_head_indexed_topk",
-    "ns_step_launches",
+    "ns_step_launches", "ns_step_batch_union", "ns_get_union",
 )
 NOALLOC_MAX_LOGITS = 1 << 20
 
@@ -91,6 +91,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "ns_sub_lm_head_indexed_topk": (I32, [P, I32, U16P, U16P, I32, I32, P, I32, P, P, P]),
         "ns_step_batch": (I32, [P, I32, P, I32, P, I32, ctypes.POINTER(I32), U16P, U16P, I32, I32, P, I32, P, P,
                                 P]),
+        "ns_step_batch_union": (I32, [P, I32, P, I32, P, I32, ctypes.POINTER(I32), U16P, U16P, I32, I32, P, I32, P,
+                                      P, P]),
+        "ns_get_union": (I32, [P] + [ctypes.POINTER(P)] * 4 + [ctypes.POINTER(I64)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -262,6 +265,38 @@ class Handle:
                                        _ptr(logits, torch.float32, "logits"), ld, _ptr(ids, torch.int32, "ids"),
                                        _ptr(vals, torch.float32, "vals"), _stream(stream)), "ns_step_batch")
         return ids, vals
+
+    def step_batch_union(self, tree_ids: Optional[torch.Tensor], verify_logits: Optional[torch.Tensor], verify_rows,
+                         W_head: torch.Tensor, hidden: torch.Tensor, k: int, logits: Optional[torch.Tensor] = None,
+                         ids: Optional[torch.Tensor] = None, vals: Optional[torch.Tensor] = None,
+                         stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        """ns_step_batch_union for sequences 0 .. B-1 (shapes as step_batch; logits [B, n, >= union capacity])."""
+        B, n = hidden.shape[0], hidden.shape[1]
+        n_tree = 0 if tree_ids is None else tree_ids.shape[1]
+        n_v = 0 if verify_logits is None else verify_logits.shape[1]
+        rows = (ctypes.c_int32 * B)(*[int(x) for x in verify_rows]) if verify_logits is not None else None
+        if ids is None:
+            ids = torch.empty((B, n, k), dtype=torch.int32, device=self.device)
+        if vals is None:
+            vals = torch.empty((B, n, k), dtype=torch.float32, device=self.device)
+        ld = logits.shape[-1] if logits is not None else 0
+        _check(self._lib.ns_step_batch_union(self._h, B, _ptr(tree_ids, torch.int32, "tree_ids"), n_tree,
+                                             _ptr(verify_logits, torch.float32, "verify_logits"), n_v, rows,
+                                             _ptr(W_head, _BF16, "W_head"), _ptr(hidden, _BF16, "hidden"), n, k,
+                                             _ptr(logits, torch.float32, "logits"), ld, _ptr(ids, torch.int32, "ids"),
+                                             _ptr(vals, torch.float32, "vals"), _stream(stream)),
+               "ns_step_batch_union")
+        return ids, vals
+
+    def get_union(self):
+        """Views (ids int32 [cap], count int32 [1], bitmap int32 [ceil(V/32)], packed int16 [cap, H]) and cap."""
+        p = [ctypes.c_void_p() for _ in range(4)]
+        cap = ctypes.c_int64()
+        _check(self._lib.ns_get_union(self._h, *[ctypes.byref(x) for x in p], ctypes.byref(cap)), "ns_get_union")
+        c, m = self.cfg, int(cap.value)
+        nwords = (c.V + 31) // 32
+        return (_view(p[0].value, (m,), "<i4", self.device), _view(p[1].value, (1,), "<i4", self.device),
+                _view(p[2].value, (nwords,), "<i4", self.device), _view(p[3].value, (m, c.H), "<i2", self.device), m)
 
     def state_update(self, seq: int, tree_ids: Optional[torch.Tensor], verify_logits: Optional[torch.Tensor],
                      verify_row: int = 0, stream=None) -> None:
