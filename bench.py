@@ -875,12 +875,65 @@ def run_ours(args):
                              "ctx_plus_ext_step_us": 1e3 * total_ms / K,
                              "note": f"64 steps from the initial state each; the headline is the first {K} steps"}
 
-        # two-stream pipeline (MicroSpec §3.3): the gather of W_head[I_t, :] on a
-        # copy stream while a stand-in draft backbone runs on the compute
-        # stream, which waits for the gather only before the projection.
-        # Stand-ins: one Llama-3-8B-sized decoder layer's weights read once by
-        # the n tree tokens (HBM-bound, 4 x H^2 + 3 x H x 14336 bf16 weights),
-        # and four 2048^3 bf16 GEMMs (tensor-bound).
+        # an EAGLE-style draft phase on one step's I_t: D = 6 tree levels, each
+        # a projection of its own hidden rows over the same I_t.  Four ways to
+        # serve it, each a decode step (state update included) timed like the
+        # policies: the slot buffer (copy the rows new to I_t, then D
+        # projections over the slots); one full repack then D projections; D
+        # fused repack + projection calls; D indexed products (nothing packed).
+        depth = 6
+
+        def level_hid(t, d):
+            return hid_d[(t * depth + d) % T]
+
+        def upd(t):
+            u = t % T
+            h.state_update(0, trees_d[u], verify_d[u], vrows[u])
+
+        def dp_slots(t):
+            upd(t)
+            h.gather_new_head_rows(0, W_d)
+            for d in range(depth):
+                h.slot_lm_head_logits_topk(0, level_hid(t, d), k, logits=logits, ids=ids, vals=vals)
+
+        def dp_one_repack(t):
+            upd(t)
+            h.gather_head_rows(0, W_d)
+            for d in range(depth):
+                h.sub_lm_head_logits_topk(0, level_hid(t, d), k, logits=logits, ids=ids, vals=vals)
+
+        def dp_fused_each(t):
+            upd(t)
+            for d in range(depth):
+                h.gather_sub_lm_head_topk(0, W_d, level_hid(t, d), k, logits=logits, ids=ids, vals=vals)
+
+        def dp_indexed_each(t):
+            upd(t)
+            for d in range(depth):
+                h.sub_lm_head_indexed_topk(0, W_d, level_hid(t, d), k, logits=logits, ids=ids, vals=vals)
+
+        T3 = min(T, 32)
+        extra["draft_phase"] = {
+            "depth": depth,
+            "slots_us": policy_us(slot_init, dp_slots, T3),
+            "one_repack_us": policy_us(init, dp_one_repack, T3),
+            "fused_repack_each_us": policy_us(init, dp_fused_each, T3),
+            "indexed_each_us": policy_us(init, dp_indexed_each, T3),
+            "note": f"per decode step: state update + {depth} projections of n={n} rows with top-{k}, "
+                    f"{T3} steps from the prefill state",
+        }
+        if h.get_error() != 0:
+            raise RuntimeError("device error flags set during the draft-phase steps")
+
+        # two-stream pipeline (MicroSpec §3.3): the gather of W_head[I_t, :] on
+        # a copy stream while the draft backbone runs on the compute stream,
+        # which waits for the gather only before the first projection.  The
+        # backbone stands in for an EAGLE draft phase: `depth` levels, each one
+        # Llama-3-8B-sized decoder layer whose weights (4 x H^2 + 3 x H x 14336
+        # bf16, 436 MB) are read once by the n tree rows, then that level's
+        # projection.  NanoSpec's 1.4 ms backbone is this on a GPU with about
+        # a third of GB300's HBM bandwidth.  A second stand-in is
+        # tensor-bound: four 2048^3 bf16 GEMMs before the first projection.
         copy_s = torch.cuda.Stream()
         n_layer = 4 * H + 3 * 14336
         W_layer = torch.empty((n_layer, H), dtype=torch.bfloat16, device=dev).normal_(0.0, 0.02)
@@ -898,27 +951,57 @@ def run_ours(args):
         def gather():
             h.gather_head_rows(0, W_d, copy_stream=torch.cuda.current_stream())
 
-        def project():
-            h.sub_lm_head_logits_topk(0, hid_d[0], k, logits=logits, ids=ids, vals=vals)
+        def project(d=0):
+            h.sub_lm_head_logits_topk(0, hid_d[d % T], k, logits=logits, ids=ids, vals=vals)
 
-        def overlapped(backbone):
+        def eagle_serial():
+            gather()
+            for d in range(depth):
+                layer()
+                project(d)
+
+        def eagle_overlapped():
             cur = torch.cuda.current_stream()
             copy_s.wait_stream(cur)
             h.gather_head_rows(0, W_d, copy_stream=copy_s)
-            backbone()
+            for d in range(depth):
+                layer()
+                if d == 0:
+                    cur.wait_stream(copy_s)
+                project(d)
+
+        def square_serial():
+            square()
+            gather()
+            project()
+
+        def square_overlapped():
+            cur = torch.cuda.current_stream()
+            copy_s.wait_stream(cur)
+            h.gather_head_rows(0, W_d, copy_stream=copy_s)
+            square()
             cur.wait_stream(copy_s)
             project()
 
         init()
         h.build_active_vocab(0)
-        us_gather, us_project = graph_us(gather), graph_us(project)
-        ov = {"active": m0, "gather_us": us_gather, "project_us": us_project}
-        for name, bb in (("decoder_layer", layer), ("square_gemms", square)):
-            us_bb = graph_us(bb)
-            us_serial = graph_us(lambda: (bb(), gather(), project()))
-            us_ov = graph_us(lambda: overlapped(bb))
-            ov[name] = {"backbone_us": us_bb, "serial_us": us_serial, "overlapped_us": us_ov,
-                        "gather_hidden_frac": (us_serial - us_ov) / us_gather}
+        us_project = graph_us(project)
+        us_layer = graph_us(layer)
+        us_sq = graph_us(square)
+        ov = {"active": m0, "project_us": us_project, "layer_us": us_layer, "depth": depth,
+              "eagle_backbone_us": depth * us_layer, "square_gemms_us": us_sq, "by_copy_ctas": {}}
+        for ctas in (0, 152, 38, 16):
+            h.set_copy_ctas(ctas)
+            us_gather = graph_us(gather)
+            e_ser, e_ov = graph_us(eagle_serial), graph_us(eagle_overlapped)
+            s_ser, s_ov = graph_us(square_serial), graph_us(square_overlapped)
+            ov["by_copy_ctas"][str(ctas) if ctas else "default"] = {
+                "gather_us": us_gather,
+                "eagle_serial_us": e_ser, "eagle_overlapped_us": e_ov,
+                "eagle_gather_hidden_frac": (e_ser - e_ov) / us_gather,
+                "square_serial_us": s_ser, "square_overlapped_us": s_ov,
+                "square_gather_hidden_frac": (s_ser - s_ov) / us_gather}
+        h.set_copy_ctas(0)
         extra["copy_stream_overlap"] = ov
         del W_layer, y_layer, xs, ys
         dense_out = torch.empty((n, V), dtype=torch.bfloat16, device=dev)

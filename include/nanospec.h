@@ -294,6 +294,15 @@ NS_API ns_status ns_sub_lm_head_indexed_topk(ns_handle *h, int32_t seq, const ui
                                              ns_stream stream);
 
 /*
+ * CTAs of the copy kernels (ns_gather_head_rows, ns_gather_new_head_rows)
+ * from now on; 0 restores the default (four per SM for the gather, two for
+ * the slot-row copy).  A copy meant to run beside a backbone that fills the
+ * GPU can take a few CTAs, which find room while the backbone's kernels hold
+ * the rest.  Results do not depend on it.  NS_ERR_ARG for ctas < 0.
+ */
+NS_API ns_status ns_set_copy_ctas(ns_handle *h, int32_t ctas);
+
+/*
  * Slot-stable packed buffer: the incremental reading of NanoSpec's
  * "Avoiding Sparse Computation via Asynchronous Gathering" (only the weights
  * of newly active tokens are gathered into the pre-allocated contiguous

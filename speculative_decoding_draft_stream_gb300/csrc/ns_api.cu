@@ -433,6 +433,13 @@ ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t 
   return cuda_status(e);
 }
 
+ns_status ns_set_copy_ctas(ns_handle *h, int32_t ctas) {
+  if (!h || ctas < 0) return NS_ERR_ARG;
+  h->ggrid = ctas > 0 ? ctas : 4 * h->num_sms;
+  h->sgrid = ctas > 0 ? ctas : 2 * h->num_sms;
+  return NS_OK;
+}
+
 ns_status ns_gather_new_head_rows(ns_handle *h, int32_t seq, const uint16_t *d_W_head, ns_stream copy_stream,
                                   ns_event done) {
   if (!valid_seq(h, seq) || !d_W_head || !aligned16(d_W_head)) return NS_ERR_ARG;

@@ -35,7 +35,7 @@ EXPORTED = (
     "ns_dense_lm_head_topk", "ns_get_active", "ns_get_state", "ns_get_error", "ns_state_update",
     "ns_gather_sub_lm_head_topk", "ns_trace_events", "ns_dense_lm_head_topk_noalloc", "ns_gather_new_head_rows",
     "ns_slot_lm_head_logits_topk", "ns_step_slots", "ns_get_slots", "ns_step_batch", "ns_sub_lm_head_indexed_topk",
-    "ns_step_launches", "ns_step_batch_union", "ns_get_union",
+    "ns_step_launches", "ns_step_batch_union", "ns_get_union", "ns_set_copy_ctas",
 )
 NOALLOC_MAX_LOGITS = 1 << 20
 
@@ -69,6 +69,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "ns_destroy": (I32, [P]),
         "ns_device_bytes": (I64, [P]),
         "ns_step_launches": (I32, [P]),
+        "ns_set_copy_ctas": (I32, [P, I32]),
         "ns_stream_init": (I32, [P, I32, P, I32, P, P]),
         "ns_stream_append": (I32, [P, I32, P, I32, P, I32, I32, P]),
         "ns_build_active_vocab": (I32, [P, I32, P]),
@@ -318,6 +319,10 @@ class Handle:
                                                     _ptr(ids, torch.int32, "ids"), _ptr(vals, torch.float32, "vals"),
                                                     _stream(stream)), "ns_gather_sub_lm_head_topk")
         return ids, vals
+
+    def set_copy_ctas(self, ctas: int) -> None:
+        """CTAs of the copy kernels (0: the default)."""
+        _check(self._lib.ns_set_copy_ctas(self._h, ctas), "ns_set_copy_ctas")
 
     # -- the slot-stable buffer (incremental gather) ---------------------------
     def gather_new_head_rows(self, seq: int, W_head: torch.Tensor, copy_stream=None,

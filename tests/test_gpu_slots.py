@@ -185,3 +185,45 @@ def test_slots_follow_any_update_schedule(pkg):
         h.gather_new_head_rows(0, W_dev)
         check_slots(h, 0, osl, osl.update(ost.active(), W), W)
         assert h.get_error() == 0
+
+
+def _draft_phase(pkg, cfg, steps, depth=6):
+    """An EAGLE-style draft phase on the slot buffer: per step one state
+    update and one slot gather, then `depth` projections of the same I_t
+    with different hidden rows (one per level of the draft tree), each
+    against the oracle."""
+    wl = Workload(cfg)
+    W = wl.w_head()
+    W_dev = dev_bf16(W)
+    with _handle(pkg, cfg, wl.prompt_len(0)) as h:
+        prompt, Z = wl.prompt(0), wl.prefill_logits(0)
+        ost = oracle.OracleStream(cfg.V, cfg.W_max, cfg.K_pre, cfg.K_ver)
+        ost.init(prompt, Z)
+        osl = oracle.OracleSlots(cfg.W_max, cfg.H)
+        h.stream_init(0, dev_i32(prompt), dev_f32(Z))
+        h.build_active_vocab(0)
+        h.gather_new_head_rows(0, W_dev)
+        osl.update(ost.active(), W)
+        logits = torch.zeros((cfg.n_tree, cfg.W_max), dtype=torch.float32, device="cuda")
+        trees = wl.trees(0)
+        for t in range(steps):
+            vb, vr = wl.verify_logits(0, t), wl.verify_row(0, t)
+            h.state_update(0, dev_i32(trees[t]), dev_f32(vb), vr)
+            h.gather_new_head_rows(0, W_dev)
+            ost.append(trees[t], vb, vr)
+            I = check_state(h, 0, ost, full=False)
+            pairs = osl.update(I, W)
+            check_slots(h, 0, osl, pairs, W, full=False)
+            for d in range(depth):
+                hid = wl.hiddens(0, cfg.steps + t * depth + d)
+                ids, vals = h.slot_lm_head_logits_topk(0, dev_bf16(hid), cfg.k, logits=logits)
+                check_slot_projection(logits, ids, vals, hid, osl, I, cfg.k)
+        assert h.get_error() == 0
+
+
+def test_one_gather_serves_a_draft_phase(pkg):
+    _draft_phase(pkg, MID, steps=6)
+
+
+def test_one_gather_serves_a_draft_phase_full_size(pkg):
+    _draft_phase(pkg, get_config("llama3_8b_v128256_h4096"), steps=3)
