@@ -83,6 +83,7 @@ void layout(ns_handle *h, Carver &cv) {
     s.active = cv.take<int32_t>(c.W_max);
     s.count = cv.take<int32_t>(1);
     s.length = cv.take<long long>(2);
+    s.active_len = cv.take<long long>(1);
     s.packed = cv.take<uint16_t>((size_t)c.W_max * c.H);
     s.logits = cv.take<float>((size_t)ns::kProjBN * d.ld_scratch);
     s.first = c.K_pre > 0 ? cv.take<int32_t>(c.V) : nullptr;

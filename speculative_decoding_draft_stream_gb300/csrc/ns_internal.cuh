@@ -30,6 +30,7 @@ struct SeqDev {
   uint32_t *bitmap;   // [nwords_pad] bit i%32 of word i/32 <=> id i in window
   int32_t *active;    // [W_max] I_t ascending
   int32_t *count;     // [1] |I_t|
+  long long *active_len;  // [1] |S| when active and count were last built (another |S|: they are stale)
   long long *length;  // [2] |S|, then |S| mod W_max (the ring slot of the next entry)
   uint16_t *packed;   // [W_max x H] bf16 rows W_head[I_t[j], :]
   float *logits;      // [kProjBN x ld_scratch] fp32 logits when the caller passes none
@@ -71,7 +72,7 @@ __host__ __device__ inline SeqDev seq_at(SeqDev s, long long off) {
   move_ptr(s.first, off), move_ptr(s.cand, off), move_ptr(s.sinit, off), move_ptr(s.cand_k, off);
   move_ptr(s.cand_i, off), move_ptr(s.slice_ticket, off), move_ptr(s.slot_id, off), move_ptr(s.held, off);
   move_ptr(s.slot_meta, off), move_ptr(s.new_slot, off), move_ptr(s.new_id, off), move_ptr(s.slot_rows, off);
-  move_ptr(s.gbar, off), move_ptr(s.vcand_k, off), move_ptr(s.vcand_i, off);
+  move_ptr(s.gbar, off), move_ptr(s.vcand_k, off), move_ptr(s.vcand_i, off), move_ptr(s.active_len, off);
   return s;
 }
 

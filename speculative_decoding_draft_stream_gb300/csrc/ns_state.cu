@@ -173,6 +173,7 @@ __global__ void init_reset_kernel(SeqDev s, Dims d) {
     s.length[0] = 0;
     s.length[1] = 0;
     *s.count = 0;
+    *s.active_len = 0;  // the empty I_t matches the empty stream
     s.slot_meta[0] = 0;
     s.slot_meta[1] = 0;
     *s.gbar = 0ull;
@@ -681,8 +682,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) append_kernel(SeqDev s, Dims
   }
   __syncthreads();
 
-  if (BUILD && have_bits)
+  if (BUILD && have_bits) {
     compact_bitmap(s_bits, d.nwords, d.nwords_pad, s_nzw, s_nzo, s.active, s.count, d.W_max, err, sh_scan);
+    if (tid == 0 && s.active_len) *s.active_len = len1;
+  }
 }
 
 __global__ void __launch_bounds__(kStateThreads) build_kernel(SeqDev s, Dims d, uint32_t *err) {
@@ -695,6 +698,7 @@ __global__ void __launch_bounds__(kStateThreads) build_kernel(SeqDev s, Dims d, 
   for (int q = threadIdx.x; q < d.nwords_pad / 4; q += blockDim.x) s_dyn4[q] = g4[q];
   __syncthreads();
   compact_bitmap(s_bits, d.nwords, d.nwords_pad, s_nzw, s_nzo, s.active, s.count, d.W_max, err, sh_scan);
+  if (threadIdx.x == 0 && s.active_len && s.length) *s.active_len = s.length[0];
 }
 
 // The union of several sequences' windows: word w of every bitmap ORed.

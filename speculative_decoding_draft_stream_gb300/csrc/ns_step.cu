@@ -7,35 +7,44 @@
 // and Verify Candidates), §3.3 (GPU-resident state, the contiguous sub-head
 // buffer) and §3.1 Eq. 1 restricted to I_t.
 //
-// Why one launch.  The state update moves almost no bytes but is a chain of
-// dependent steps (read the verify row, rank it, merge, append, update the
-// bitmap, compact), and the product can only start once I_t is known.  Here
-// every CTA of the product's grid takes part in the state update, so the
-// chain runs on the whole GPU, and the row reads of the product start at the
-// first cycle: I_t differs from I_{t-1} by the few ids that enter or leave,
-// so each CTA prefetches into L2 the rows it read in the previous step while
-// the state update runs.
+// Why the projection does not wait for I_t.  The state update moves almost
+// no bytes but is a chain of dependent steps (read the verify row, rank it,
+// merge across the grid, append, evict, compact), while the product moves
+// the bytes.  Each logit is one dot product, so where a column sits in I_t
+// does not change its value, and I_t differs from I_{t-1} only by the ids
+// that enter (this step's draft and verify candidates) and leave.  So the
+// product starts at the first cycle on what is already known:
+//   * one work item per 128 ids of I_{t-1} (read before anything changes);
+//   * one item for the draft-tree ids (inputs of the step);
+//   * the few verify Top-K ids (K_ver of them) by CUDA-core dot products,
+//     once the grid has ranked the verify row.
+// When the state update has produced I_t, every column is written at the
+// position of its id in I_t: an id of I_{t-1} that stays by its old item,
+// an id that enters by the draft item or the verify products (the first
+// candidate that holds it), an id that leaves by nobody, so each column of
+// I_t is written exactly once.  The packed buffer (W_head[I_t, :] in I_t
+// order) is filled by bulk row copies that run beside the top-k.
 //
-// Phase A (every CTA, from the first cycle):
-//   * bulk copies of the window bitmap, the ring and |S| into shared memory;
-//   * its slice of the verify row: the slice's Top-K_ver, sorted, to global;
-//   * C_draft from the tree ids (warp 1);
-//   * L2 prefetch of the rows of its tiles in the previous I_t, and of the
-//     tree ids' rows;
-//   * the ids of the ring entries that may leave the window, and for each the
-//     last position at which it occurs in the window (from the ring copy).
-// Grid barrier: one arrival per CTA on a 64-bit counter (bounded wait).
-// Phase B (every CTA computes the same thing):
-//   * merge of every CTA's Top-K list into C_ver;
-//   * what enters (appended) and what leaves (evicted with no later
-//     occurrence and not appended again): the updated bitmap in shared memory;
-//   * block scan of the bitmap into I_t positions and the ids of its own tiles;
-//   * the last CTA writes the ring, |S|, the window counts and the changed
-//     bitmap words; each CTA writes its share of I_t.
-// Then the tcgen05 tile (ns_umma_tile.cuh) on the CTA's tiles.
+// A CTA runs three groups of warps side by side:
+//   * tile group, warps 0-1 and 4-11: its cluster's items (tcgen05 tiles
+//     split over H across the cluster: TMA hidden loads, cp.async row
+//     gathers into the 128-byte-swizzled layout, MMA into tensor memory,
+//     split-K partials summed through distributed shared memory in rank
+//     order), then the logits writes;
+//   * verify group, warps 2-3: the verify ids' logits;
+//   * state group, warps 12-15: the state update, computed identically by
+//     every CTA (its slice of the verify row, a grid barrier, the merge of
+//     all slices into C_ver, the window update and the compaction), then its
+//     share of I_t and of the packed buffer.
+// The groups meet through mbarriers (old-state reads done; C_ver known; I_t
+// known; the stage ring free), so none waits at another's block barriers.  Warps 0-11 then take the second grid
+// barrier together and rank whole rows.
 //
-// Reads of the old state all happen before a CTA arrives at the grid barrier,
-// writes of the new state all after it, so no CTA sees a half-updated state.
+// Reads of the old state (I_{t-1}, |I_{t-1}|, the bitmap, the ring, |S|)
+// all happen before a CTA arrives at the first grid barrier, writes of the
+// new state all after it.  Every wait is bounded (about a second); a wait
+// that runs out sets NS_FLAG_TIMEOUT and the kernel still follows the same
+// barrier sequence.
 #include <cuda.h>
 
 #include "ns_umma_tile.cuh"
@@ -43,29 +52,51 @@
 namespace ns {
 namespace {
 
-constexpr int kStepWarps = kUThreads / kWarp;
+constexpr int kSThreads = 512;                        // the whole CTA
+constexpr int kKThreads = 384;                        // warps 0-11: the second grid barrier and the row top-k
+constexpr int kTGroup = 320;                          // tile group: warps 0-1 and 4-11
+constexpr int kVGroup = 64;                           // verify group: warps 2-3
+constexpr int kSgThreads = kSThreads - kKThreads;     // state group: warps 12-15
+constexpr int kSgWarps = kSgThreads / kWarp;
+constexpr int kKWarps = kKThreads / kWarp;
+constexpr int kBarT = 1, kBarS = 2, kBarK = 3;        // named barriers of the groups
+constexpr int kVerPairs = 16;                         // most (verify id, hidden row) products of one CTA
+constexpr int kCopyOff = 8192;                        // packed-copy staging in the ring, past the top-k lists
+constexpr int kSStages = 6;                           // stage ring of the tiles
+constexpr int kSRing = kSStages * kStage;
+constexpr int kMaxItemsPerCluster = 2;
+constexpr int kFRows = (kUN + 3) / 4;                 // most hidden rows one CTA sums (clusters of >= 4)
+constexpr int kFBytes = kFRows * kUM * 4;
+constexpr int kStepMiscBytes = 1536;                  // barriers, TMEM slot, flags, the items' row ids
 constexpr int kMaxAppendStep = NS_MAX_ROWS + NS_MAX_SELECT_K;
-constexpr int kStepHash = 256;  // > the distinct ids one step appends or evicts (2 x 80)
-constexpr int kMaxTilesPerCluster = 4;
-constexpr int kFilterWords = 128;  // 4096-bit filter of the evictable ids (hashed), ahead of the table
-static_assert(kMaxStepCtas <= kStepWarps * kWarp, "the Top-K merge takes one list per lane of 8 warps");
-static_assert(kMaxTilesPerCluster * ((kUM + 3) / 4) <= 4 * kWarp, "the gather warps hold the prefetched row ids");
-constexpr long long kBarrierNs = 1000000000LL;    // grid barrier gives up after ~1 s
+constexpr int kVerRow0 = NS_MAX_ROWS;                 // writer-row code of verify id v: kVerRow0 + v
+constexpr int kStepHash = 256;                        // > the distinct ids one step appends or evicts (2 x 80)
+constexpr int kHashArrays = 7;                        // key, count, ev, ap, writer row, enters, changed word
+constexpr int kMaxSmem = 232448;                      // dynamic shared memory one CTA can take
+constexpr long long kBarrierNs = 1000000000LL;        // grid barrier gives up after ~1 s
+static_assert(kMaxStepCtas <= kSgWarps * 2 * kWarp, "the C_ver merge takes two lists per lane of the state warps");
+static_assert(kPartBytes <= kSRing, "partial tile fits in the stage ring");
+static_assert((kKWarps + 1) * 2 * NS_MAX_TOPK * 4 + 2 * NS_MAX_TOPK * 4 <= kCopyOff, "top-k lists before the staging");
+static_assert(kMaxItemsPerCluster * kUM * 4 + 512 <= kStepMiscBytes, "row ids fit the misc area");
+static_assert(kUM == 128 && kTGroup >= 2 * kUM, "logits writes: one column per thread, two row groups");
 
 struct StepArgs {
-  UmmaArgs u;                 // the tiles' part (W_head, hiddens, logits, candidates, outputs, error word)
+  UmmaArgs u;                 // W_head, hiddens, logits, outputs, error word
   int32_t *ring;
   uint32_t *counts;
   uint32_t *bitmap;
   int32_t *active;
   int32_t *count;
   long long *length;
+  long long *active_len;      // |S| when active/count were built
+  uint16_t *packed;
+  const uint16_t *hid;        // hidden rows [n x H] (the verify products read them directly)
   unsigned long long *gbar;   // grid barrier counter
   uint32_t *vk, *vi;          // [CTAs x K_ver] each CTA's verify Top-K (order keys, ids)
   const int32_t *tree;
   int32_t n_tree;
   const float *zrow;          // the verify row (null when K_ver = 0)
-  int32_t K, nwords_pad, ring_words, tiles_per_cluster, vec;
+  int32_t K, nwords_pad, ring_words, items_per_cluster, t_max, vec;
   int32_t probe;              // launch check only: every CTA returns at once
 };
 
@@ -91,16 +122,45 @@ __device__ __forceinline__ float ld_stream_f32(const float *p) {
   asm volatile("ld.global.cs.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
 }
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+// Arrival on a barrier of a CTA of this cluster (its shared::cluster address),
+// releasing this thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a phase completed by arrivals from the cluster's CTAs.
+static __device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint32_t *err) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(err, NS_FLAG_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
 }
 
-// Every CTA of the (co-resident) grid arrives once; returns false on every
-// thread when the wait ran out (NS_FLAG_TIMEOUT is set).  The counter only
-// grows by the grid size per barrier, so generation g ends at (g + 1) * P.
-__device__ bool grid_barrier(unsigned long long *ctr, unsigned long long P, uint32_t *err, int *s_ok) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
+// One arrival per CTA (by `leader`, after a barrier of its group) on a 64-bit
+// counter that only grows by the grid size per barrier, so generation g ends
+// at (g + 1) * P.  Returns false on every thread of the group when the wait
+// ran out (NS_FLAG_TIMEOUT is set).
+__device__ bool grid_barrier(unsigned long long *ctr, unsigned long long P, uint32_t *err, int *s_ok, int bar_id,
+                             int threads, bool leader) {
+  named_sync(bar_id, threads);
+  if (leader) {
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
     const unsigned long long old = atomicAdd(ctr, 1ull);
     const unsigned long long target = (old / P + 1) * P;
@@ -118,7 +178,7 @@ __device__ bool grid_barrier(unsigned long long *ctr, unsigned long long P, uint
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
     *s_ok = ok;
   }
-  __syncthreads();
+  named_sync(bar_id, threads);
   return *s_ok != 0;
 }
 
@@ -134,6 +194,24 @@ __device__ __forceinline__ int select_bit(uint32_t w, int r) {
   if (r >= c) { r -= c; b += 2; w >>= 2; }
   if (r >= (int)(w & 1u)) b += 1;
   return b;
+}
+
+// Id at position p (< |I_t|) of I_t: the last 4-word group whose count of
+// earlier ids is <= p, then the word and the bit.
+__device__ __forceinline__ int nth_id(const uint32_t *bits, const int32_t *goff, int ng, int p) {
+  int lo_g = 0, hi_g = ng - 1;
+  while (lo_g < hi_g) {
+    const int mid = (lo_g + hi_g + 1) >> 1;
+    if (goff[mid] <= p) lo_g = mid;
+    else hi_g = mid - 1;
+  }
+  int r = p - goff[lo_g], wi = 4 * lo_g;
+  uint32_t w = bits[wi];
+  while (r >= __popc(w)) {
+    r -= __popc(w);
+    w = bits[++wi];
+  }
+  return wi * 32 + select_bit(w, r);
 }
 
 // Slot of `id` in the open-addressing table (inserted when absent); -1 when
@@ -158,13 +236,66 @@ __device__ __forceinline__ int hash_find(const int *keys, int id) {
   return -1;
 }
 
-// Word offsets of the phase A/B arrays inside the stage ring (the bulk-copy
-// destinations and the bitmap's uint4 reads need 16-byte alignment).
+// One warp: the K best entries of `nl` (<= 64) lists sorted best first, K
+// entries each (list l at lk/li[l * K]); lane l follows lists l and l + 32.
+// Winners go to ok/oi[r] (lane 0 writes).
+__device__ __forceinline__ void warp_merge_lists64(const uint32_t *lk, const uint32_t *li, int nl, int K,
+                                                   uint32_t *ok, uint32_t *oi) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  int pa = 0, pb = 0;
+  const int la = lane, lb = lane + kWarp;
+#pragma unroll 1
+  for (int r = 0; r < K; ++r) {
+    uint32_t ak = 0u, ai = (uint32_t)kEmptyId, bk = 0u, bi = (uint32_t)kEmptyId;
+    if (la < nl && pa < K) {
+      ak = lk[la * K + pa];
+      ai = li[la * K + pa];
+    }
+    if (lb < nl && pb < K) {
+      bk = lk[lb * K + pb];
+      bi = li[lb * K + pb];
+    }
+    const bool take_b = bk > ak || (bk == ak && bi < ai);
+    const uint32_t hk = take_b ? bk : ak, hi = take_b ? bi : ai;
+    uint32_t wk, wi;
+    warp_best(hk, hi, wk, wi);
+    if (lane == 0) {
+      ok[r] = wk;
+      oi[r] = wi;
+    }
+    if (wk != 0u && hk == wk && hi == wi) {
+      if (take_b) ++pb;
+      else ++pa;
+    }
+  }
+  __syncwarp();
+}
+
+// Exclusive prefix sum of one int per thread over the state group.  `sh`
+// needs kSgWarps ints.
+__device__ __forceinline__ int sg_exclusive_scan(int v, int *sh, int *total) {
+  const int lane = threadIdx.x & (kWarp - 1), w = ((int)threadIdx.x - kKThreads) >> 5;
+  const int incl = warp_inclusive_scan(v);
+  if (lane == kWarp - 1) sh[w] = incl;
+  named_sync(kBarS, kSgThreads);
+  int off = 0, tot = 0;
+#pragma unroll
+  for (int q = 0; q < kSgWarps; ++q) {
+    if (q < w) off += sh[q];
+    tot += sh[q];
+  }
+  *total = tot;
+  return off + incl - v;
+}
+
+// Word offsets of the state group's arrays (the bulk-copy destinations need
+// 16-byte alignment).
 struct StepSmem {
-  int bits, ring, len, goff, vk, vi, hash, filt, wl, small, total;
+  int bits, ring, len, goff, vk, vi, hash, wl, small, share, total;
 };
 __host__ __device__ inline int round4(int x) { return (x + 3) & ~3; }
-__host__ __device__ inline StepSmem step_smem(int nwords_pad, int ring_words, int P, int K) {
+__host__ __device__ inline int share_of(int W, int P) { return (W + P - 1) / P; }
+__host__ __device__ inline StepSmem step_smem(int nwords_pad, int ring_words, int W, int P, int K) {
   StepSmem L;
   L.bits = 0;
   L.ring = L.bits + nwords_pad;                 // nwords_pad and ring_words are multiples of 4
@@ -173,58 +304,124 @@ __host__ __device__ inline StepSmem step_smem(int nwords_pad, int ring_words, in
   L.vk = L.goff + round4(nwords_pad / 4);
   L.vi = L.vk + round4(P * K);
   L.hash = L.vi + round4(P * K);
-  L.filt = L.hash + 4 * kStepHash;
-  L.wl = L.filt + kFilterWords;
-  L.small = L.wl + 2 * (kStepWarps + 1) * NS_MAX_SELECT_K + 2 * NS_MAX_SELECT_K;
-  L.total = L.small + round4(NS_MAX_ROWS + 2 * kMaxAppendStep + 4 + kStepWarps);
+  L.wl = L.hash + kHashArrays * kStepHash;
+  L.small = L.wl + 2 * (kSgWarps + 1) * NS_MAX_SELECT_K + 2 * NS_MAX_SELECT_K;
+  L.share = L.small + round4(NS_MAX_ROWS + 3 * kMaxAppendStep + 8 + kSgWarps + 3 * kVerPairs);
+  L.total = L.share + round4(share_of(W, P));
   return L;
+}
+__host__ __device__ inline int step_smem_bytes(const StepSmem &L) {
+  return 1024 + kSRing + kMaxItemsPerCluster * kFBytes + kStepMiscBytes + 4 * L.total;
 }
 
 template <int kCL>
-__global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kUThreads, 1)
-    step_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmP, StepArgs a) {
+__global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
+    step_kernel(const __grid_constant__ CUtensorMap tmH, StepArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) unsigned long long s_sbar;
-  __shared__ int s_tiles[kMaxTilesPerCluster * kUM];  // the row ids of this CTA's tiles
   if (a.probe) return;
 
-  const UmmaSmem S = umma_smem(smem_raw);
   const UmmaArgs &u = a.u;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool tgrp = warp < 2 || (warp >= 4 && warp < kKWarps);  // tile group
+  const bool vgrp = warp == 2 || warp == 3;                      // verify group
+  const bool sgrp = warp >= kKWarps;                             // state group
+  const int ttid = warp < 2 ? tid : tid - kVGroup;               // index in the tile group
+  const int stid = tid - kKThreads;                              // index in the state group
   const uint32_t crank = cluster_rank();
   const int P = (int)gridDim.x, cta = (int)blockIdx.x;
   const int cid = cta / kCL, ncid = P / kCL;
-  const int V = u.V, W = u.W_max, K = a.K, n_tree = a.n_tree;
+  const int V = u.V, W = u.W_max, K = a.K, n_tree = a.n_tree, H = u.H;
   const bool writer = cta == P - 1;
-  // Phase A/B working set, inside the stage ring (free until the tiles run).
-  const StepSmem L = step_smem(a.nwords_pad, a.ring_words, P, K);
-  int32_t *wbase = reinterpret_cast<int32_t *>(S.gbase);
+
+  // ---- shared memory ----------------------------------------------------------
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte-swizzled stages need 1024-byte alignment
+  uint8_t *gbase = smem_raw + (base - raw);
+  float *Fbuf = reinterpret_cast<float *>(gbase + kSRing);  // [items][kFRows][kUM] summed tiles
+  uint8_t *misc = gbase + kSRing + kMaxItemsPerCluster * kFBytes;
+  const uint32_t bar_full = smem_u32(misc), bar_empty = bar_full + 8 * kSStages;
+  const uint32_t bar_acc = bar_empty + 8 * kSStages, bar_pready = bar_acc + 8, bar_pdone = bar_pready + 8;
+  const uint32_t bar_old = bar_pdone + 8, bar_cver = bar_old + 8, bar_state = bar_cver + 8;
+  const uint32_t bar_ring = bar_state + 8, bar_copy = bar_ring + 8, sbar = bar_copy + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc + 256);
+  int *s_flag = reinterpret_cast<int *>(misc + 272);   // [1] state failed, [2], [3] barrier words
+  int *s_tiles = reinterpret_cast<int *>(misc + 512);  // [items][kUM] ids of the items' rows (-1: none)
+  int32_t *wbase = reinterpret_cast<int32_t *>(misc + kStepMiscBytes);
+  const StepSmem L = step_smem(a.nwords_pad, a.ring_words, W, P, K);
   uint32_t *s_bits = reinterpret_cast<uint32_t *>(wbase + L.bits);
   int32_t *s_ring = wbase + L.ring;
   long long *s_len = reinterpret_cast<long long *>(wbase + L.len);
   int32_t *s_goff = wbase + L.goff;
-  int *h_key = wbase + L.hash, *h_last = h_key + kStepHash, *h_ev = h_last + kStepHash, *h_ap = h_ev + kStepHash;
-  uint32_t *s_filt = reinterpret_cast<uint32_t *>(wbase + L.filt);
-  uint32_t *wl_k = reinterpret_cast<uint32_t *>(wbase + L.wl), *wl_i = wl_k + (kStepWarps + 1) * NS_MAX_SELECT_K;
-  uint32_t *res_k = wl_i + (kStepWarps + 1) * NS_MAX_SELECT_K, *res_i = res_k + NS_MAX_SELECT_K;
-  int *s_tree = wbase + L.small, *s_app = s_tree + NS_MAX_ROWS, *s_evid = s_app + kMaxAppendStep;
-  int *s_misc = s_evid + kMaxAppendStep, *sh_scan = s_misc + 4;
+  int *h_key = wbase + L.hash, *h_cnt = h_key + kStepHash, *h_ev = h_cnt + kStepHash, *h_ap = h_ev + kStepHash;
+  int *h_wrow = h_ap + kStepHash, *h_ent = h_wrow + kStepHash, *h_chg = h_ent + kStepHash;
+  uint32_t *wl_k = reinterpret_cast<uint32_t *>(wbase + L.wl), *wl_i = wl_k + (kSgWarps + 1) * NS_MAX_SELECT_K;
+  uint32_t *res_k = wl_i + (kSgWarps + 1) * NS_MAX_SELECT_K, *res_i = res_k + NS_MAX_SELECT_K;
+  int *s_tree = wbase + L.small, *s_app = s_tree + NS_MAX_ROWS, *s_arow = s_app + kMaxAppendStep;
+  int *s_evid = s_arow + kMaxAppendStep, *s_misc = s_evid + kMaxAppendStep, *sh_scan = s_misc + 8;
+  float *s_vdot = reinterpret_cast<float *>(sh_scan + kSgWarps);  // [kVerPairs] verify products
+  int *s_vpair = reinterpret_cast<int *>(s_vdot + kVerPairs);     // [kVerPairs] their pair index
+  int32_t *s_share = wbase + L.share;
   uint32_t *s_vk = reinterpret_cast<uint32_t *>(wbase + L.vk);
   uint32_t *s_vi = reinterpret_cast<uint32_t *>(wbase + L.vi);
-  const uint32_t sbar = smem_u32(&s_sbar);
 
-  // ---- phase A: the loads of the old state and of the verify slice ---------
+  const int nitems = a.items_per_cluster;
+  const int t_max = a.t_max;
+  const int KC = H / kUK;
+  const int nk = KC > (int)crank ? (KC - (int)crank + kCL - 1) / kCL : 0;  // this CTA's k slices
+  const int r0 = (kUN * (int)crank) / kCL, nr = (kUN * ((int)crank + 1)) / kCL - r0;  // hidden rows it sums
+
+  // ---- setup: barriers, the state group's copies, loads issued early --------
   if (tid == 0) {
+    for (int s = 0; s < kSStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1 + kGatherThreads);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_acc, 1);
+    mbar_init(bar_pready, kCL);
+    mbar_init(bar_pdone, kCL);
+    mbar_init(bar_old, 1);
+    mbar_init(bar_cver, 1);
+    mbar_init(bar_state, 1);
+    mbar_init(bar_ring, 1);
+    mbar_init(bar_copy, 1);
+    s_flag[1] = 0;
+    mbar_fence_init();
+  }
+  if (tid == kKThreads) {  // the state group's copies leave first
     mbar_init(sbar, 1);
-    umma_init_barriers(S, false);  // ends with the barrier-init fence
+    mbar_fence_init();
     mbar_expect_tx(sbar, (uint32_t)(a.nwords_pad + a.ring_words) * 4u + 16u);
     bulk_load(smem_u32(s_bits), a.bitmap, (uint32_t)a.nwords_pad * 4u, sbar);
     bulk_load(smem_u32(s_ring), a.ring, (uint32_t)a.ring_words * 4u, sbar);
     bulk_load(smem_u32(s_len), a.length, 16u, sbar);
-    tma_prefetch(&tmH);
-    tma_prefetch(&tmP);
   }
-  // this CTA's slice of the verify row: values [lo, lo + nsl)
+  if (tid == 32) tma_prefetch(&tmH);
+  // tile group: the ids of its items' rows (old items: I_{t-1}; the draft
+  // item: the tree ids) into registers now, published after the setup barrier
+  int t_id[kMaxItemsPerCluster];
+  int m_old = 0;
+  long long built_len = 0, cur_len = 0;
+  if (tgrp || vgrp) {  // compared after the setup barrier (the loads are in flight meanwhile)
+    m_old = *a.count;
+    built_len = *a.active_len;
+    cur_len = a.length[0];
+  }
+  if (tgrp) {
+#pragma unroll
+    for (int j = 0; j < kMaxItemsPerCluster; ++j) {
+      t_id[j] = -1;
+      const int it = cid + j * ncid;
+      if (ttid < kUM && j < nitems) {
+        if (it < t_max) {
+          if (it * kUM + ttid < W) t_id[j] = a.active[it * kUM + ttid];
+        } else if (it == t_max && ttid < n_tree) {
+          t_id[j] = a.tree[ttid];
+        }
+      }
+    }
+  }
+  // state group: its slice of the verify row (values [lo, lo + nsl)), one
+  // pass of eight values per thread in flight
   int lo = 0, nsl = 0;
   if (K > 0) {
     const int per = (((V + 3) / 4 + P - 1) / P) * 4;
@@ -232,384 +429,626 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kUThreads, 1)
     nsl = V - lo < per ? V - lo : per;
     if (nsl < 0) nsl = 0;
   }
-  // the first two passes (4 values per thread each) load at once
-  float x[4], x2[4];
-  auto load_pass = [&](int c0, float *v) {
+  constexpr int kPass = 8 * kSgThreads;
+  float x[8];
+  auto load_pass = [&](int c0) {
     const int n = nsl - c0;
     if (a.vec) {
-      float4 f = make_float4(__int_as_float(0x7fffffff), __int_as_float(0x7fffffff), __int_as_float(0x7fffffff),
-                             __int_as_float(0x7fffffff));
-      if (4 * tid < n) f = ld_stream_f4(a.zrow + lo + c0 + 4 * tid);
-      v[0] = f.x, v[1] = f.y, v[2] = f.z, v[3] = f.w;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float4 f = make_float4(__int_as_float(0x7fffffff), __int_as_float(0x7fffffff), __int_as_float(0x7fffffff),
+                               __int_as_float(0x7fffffff));
+        const int e = 4 * (h2 * kSgThreads + stid);
+        if (e < n) f = ld_stream_f4(a.zrow + lo + c0 + e);
+        x[4 * h2] = f.x, x[4 * h2 + 1] = f.y, x[4 * h2 + 2] = f.z, x[4 * h2 + 3] = f.w;
+      }
     } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int e = q * kUThreads + tid;
-        v[q] = e < n ? ld_stream_f32(a.zrow + lo + c0 + e) : __int_as_float(0x7fffffff);
+      for (int q = 0; q < 8; ++q) {
+        const int e = q * kSgThreads + stid;
+        x[q] = e < n ? ld_stream_f32(a.zrow + lo + c0 + e) : __int_as_float(0x7fffffff);
       }
     }
   };
-  if (nsl > 0) load_pass(0, x);
-  if (nsl > 4 * kUThreads) load_pass(4 * kUThreads, x2);
-  const int tree_id = tid < n_tree ? a.tree[tid] : 0;
-  // the previous I_t's rows of this CTA's share of its tiles (rows
-  // [128c/C, 128(c+1)/C) of each), loaded by the gather warps, which also
-  // issue the prefetches
-  const int tpc = a.tiles_per_cluster;
-  const int sh0 = (kUM * (int)crank) / kCL, shn = (kUM * ((int)crank + 1)) / kCL - sh0;
-  const int pt = tid - 4 * kWarp;
-  int pf_pos = -1, pf_id = -1, old_m = 0;
-  if (pt >= 0 && pt < shn * tpc) {
-    pf_pos = (cid + (pt / shn) * ncid) * kUM + sh0 + pt % shn;
-    if (pf_pos < W) {
-      old_m = *a.count;
-      pf_id = a.active[pf_pos];
-    }
+  int tree_id = 0;
+  if (sgrp) {
+    if (nsl > 0) load_pass(0);
+    tree_id = stid < n_tree ? a.tree[stid] : 0;
   }
-  for (int q = tid; q < kStepHash; q += kUThreads) {
-    h_key[q] = -1;
-    h_last[q] = -1;
-    h_ev[q] = 0;
-    h_ap[q] = 0;
-  }
-  for (int q = tid; q < kFilterWords; q += kUThreads) s_filt[q] = 0u;
-  if (warp == 1) tmem_alloc(smem_u32(S.tmem_slot), kTmemCols);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *S.tmem_slot;
+  const uint32_t tmem = *tmem_slot;
+  // every CTA of the cluster has initialized its barriers before the first
+  // remote arrival (the tile group waits on this before its first one)
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  const bool stale = built_len != cur_len;  // I_{t-1} was not built from the current window (then the tiles wait for I_t)
 
-  const size_t row_bytes = (size_t)u.H * 2;
-  // The rows of the previous I_t of this CTA's tiles start streaming into L2
-  // (they were loaded before the barrier above; the critical loads left first).
-  // The gather warps issue them, so the thread that arrives at the grid
-  // barrier has none outstanding.
-  if (pf_pos >= 0 && pf_pos < old_m && (unsigned)pf_id < (unsigned)V)
-    prefetch_l2(u.W + (size_t)pf_id * u.H, (uint32_t)row_bytes);
-  if (tid < n_tree) s_tree[tid] = tree_id;
-
-  // the old window: |S|, its ring slot, the entries that may leave
-  bool have = __syncthreads_and(mbar_wait(sbar, 0, u.err));
-  if (!have) mbar_wait(sbar, 0, u.err);  // a second bounded wait for the copies in flight
-  if (tid == kUThreads - 1 && cta < n_tree && (unsigned)s_tree[cta] < (unsigned)V)  // tree id c by CTA c
-    prefetch_l2(u.W + (size_t)s_tree[cta] * u.H, (uint32_t)row_bytes);
-  const long long len0 = s_len[0];
-  const int head = (int)s_len[1];
-  const long long old_start = len0 > W ? len0 - W : 0;
-  const int n_old = (int)(len0 - old_start);
-  int max_ev = n_tree + K;
-  if (max_ev > n_old) max_ev = n_old;
-  if (tid < max_ev) {  // position old_start + tid
-    const int slot = len0 > W ? (head + tid >= W ? head + tid - W : head + tid) : tid;
-    int id = s_ring[slot];
-    if ((unsigned)id >= (unsigned)V) {  // the ring only ever holds valid ids
-      if (writer) set_flag(u.err, NS_FLAG_INTERNAL | (2u << 8));
-      id = -1;
-    }
-    s_evid[tid] = id;
-    if (id >= 0) {
-      hash_insert(h_key, id);
-      const uint32_t f = ((uint32_t)id * 2654435761u) >> 20;
-      atomicOr(&s_filt[f >> 5], 1u << (f & 31));
-    }
-  }
-  __syncthreads();
-
-  // C_draft: distinct valid tree ids in first-occurrence node order (warp 1)
-  if (warp == 1) {
-    const int ta = lane < n_tree ? s_tree[lane] : 0;
-    const int tb = lane + 32 < n_tree ? s_tree[lane + 32] : 0;
-    const bool va = lane < n_tree && (unsigned)ta < (unsigned)V;
-    const bool vb = lane + 32 < n_tree && (unsigned)tb < (unsigned)V;
-    if (writer && ((lane < n_tree && !va) || (lane + 32 < n_tree && !vb))) set_flag(u.err, NS_FLAG_BAD_ID);
-    const int ka = va ? ta : -1 - lane, kb = vb ? tb : -33 - lane;
-    const unsigned ma = __match_any_sync(0xffffffffu, ka);
-    const unsigned mb = __match_any_sync(0xffffffffu, kb);
-    bool in_a = false;
-#pragma unroll 4
-    for (int j = 0; j < kWarp; ++j) in_a |= __shfl_sync(0xffffffffu, ka, j) == kb;
-    const bool keep_a = va && __ffs(ma) - 1 == lane;
-    const bool keep_b = vb && __ffs(mb) - 1 == lane && !in_a;
-    const unsigned ba = __ballot_sync(0xffffffffu, keep_a), bb = __ballot_sync(0xffffffffu, keep_b);
-    const unsigned lt = (1u << lane) - 1u;
-    if (keep_a) s_app[__popc(ba & lt)] = ta;
-    if (keep_b) s_app[__popc(ba) + __popc(bb & lt)] = tb;
-    if (lane == 0) s_misc[0] = __popc(ba) + __popc(bb);
-  }
-
-  // last position (relative to old_start) of each evictable id in the
-  // window: a filter bit first (one shared load for almost every entry), the
-  // table only for the few entries that pass it
-  for (int b0 = 0; b0 < n_old; b0 += 4 * kUThreads) {
-    int ids[4];
-    bool hit[4];
+  if (tgrp) {
+    // ======================== tile group ======================================
+    if (ttid < kUM) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int sl = b0 + q * kUThreads + tid;
-      ids[q] = sl < n_old ? s_ring[sl] : -1;
-      const uint32_t f = ((uint32_t)ids[q] * 2654435761u) >> 20;
-      hit[q] = ids[q] >= 0 && ((s_filt[f >> 5] >> (f & 31)) & 1u);
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (hit[q]) {
-        const int sl = b0 + q * kUThreads + tid;
-        const int h = hash_find(h_key, ids[q]);
-        if (h >= 0) atomicMax(&h_last[h], len0 > W ? (sl >= head ? sl - head : sl - head + W) : sl);
+      for (int j = 0; j < kMaxItemsPerCluster; ++j) {
+        const int it = cid + j * ncid;
+        int id = t_id[j];
+        if (it < t_max && it * kUM + ttid >= m_old) id = -1;  // past |I_{t-1}|
+        if ((unsigned)id >= (unsigned)V) id = -1;              // invalid tree ids are flagged by the state group
+        s_tiles[j * kUM + ttid] = id;
       }
     }
-  }
-
-  // the slice's Top-K: per pass, each warp's K best of its lanes' four
-  // values, then warp 0 merges the warps' lists with the running result
-  if (tid < K) {
-    wl_k[kStepWarps * K + tid] = 0u;  // the running Top-K starts empty
-    wl_i[kStepWarps * K + tid] = (uint32_t)kEmptyId;
-  }
-  for (int c0 = 0; c0 < nsl; c0 += 4 * kUThreads) {
-    if (c0 == 4 * kUThreads) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) x[q] = x2[q];
-    } else if (c0 > 0) {
-      load_pass(c0, x);
-    }
-    uint32_t hk[4], hi[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      hk[q] = order_key(x[q]);  // padding is NaN: key 0, never ranks
-      hi[q] = hk[q] != 0u ? (uint32_t)(a.vec ? lo + c0 + 4 * tid + q : lo + c0 + q * kUThreads + tid)
-                          : (uint32_t)kEmptyId;
-    }
-    warp_topk4(hk, hi, K, wl_k + warp * K, wl_i + warp * K);
-    __syncthreads();
-    if (warp == 0) {
-      uint32_t lk, li;
-      warp_merge_lists(wl_k, wl_i, kStepWarps + 1, K, res_k, res_i, lk, li);
-      if (lane < K) {
-        wl_k[kStepWarps * K + lane] = res_k[lane];
-        wl_i[kStepWarps * K + lane] = res_i[lane];
+    named_sync(kBarT, kTGroup);
+    if (ttid == 0) mbar_arrive(bar_old);  // this group's reads of the old state are done
+    int t_old = (m_old + kUM - 1) / kUM;
+    if (stale) {  // tiles of I_t itself, at their positions, once it is known
+      const bool okw = mbar_wait(bar_state, 0, u.err);
+      const int m_new = okw ? s_misc[3] : 0;
+      t_old = (m_new + kUM - 1) / kUM;
+      if (ttid < kUM) {
+        for (int j = 0; j < nitems; ++j) {
+          const int it = cid + j * ncid, p = it * kUM + ttid;
+          s_tiles[j * kUM + ttid] = it < t_max && p < m_new ? nth_id(s_bits, s_goff, a.nwords_pad / 4, p) : -1;
+        }
       }
+      named_sync(kBarT, kTGroup);
     }
-    __syncthreads();
-  }
-  if (tid < K) {
-    a.vk[cta * K + tid] = wl_k[kStepWarps * K + tid];
-    a.vi[cta * K + tid] = wl_i[kStepWarps * K + tid];
-  }
-
-  // ---- grid barrier: every CTA's Top-K is out, every old-state read done ---
-  bool ok = have && grid_barrier(a.gbar, (unsigned long long)P, u.err, &s_misc[3]);
-
-  // ---- phase B: C_ver, the window update, I_t ------------------------------
-  int m_act = 0;
-  if (ok) {
-    for (int q = tid; q < P * K; q += kUThreads) {
-      s_vk[q] = __ldcg(a.vk + q);
-      s_vi[q] = __ldcg(a.vi + q);
-    }
-    __syncthreads();
-    if (K > 0) {  // two rounds of list merging: 8 groups of at most 32 lists, then the 8 results
-      const int per_warp = (P + kStepWarps - 1) / kStepWarps;
-      const int l0 = warp * per_warp;
-      const int nl = P - l0 < per_warp ? (P - l0 > 0 ? P - l0 : 0) : per_warp;
-      uint32_t lk, li;
-      warp_merge_lists(s_vk + l0 * K, s_vi + l0 * K, nl, K, wl_k + warp * K, wl_i + warp * K, lk, li);
-      __syncthreads();
-      if (warp == 0) {
-        warp_merge_lists(wl_k, wl_i, kStepWarps, K, res_k, res_i, lk, li);
-        const int n_draft = s_misc[0];
-        const bool got = lane < K && res_k[lane] != 0u;
-        const int n_ver = __popc(__ballot_sync(0xffffffffu, got));
-        if (got) {
-          int y = (int)res_i[lane];
-          if ((unsigned)y >= (unsigned)V) {  // cannot happen for a well-formed merge
-            if (writer) set_flag(u.err, NS_FLAG_INTERNAL | (1u << 8));
-            y = 0;
+    bool cluster_ready = false;
+    int iter = 0;
+    for (int j = 0; j < nitems; ++j) {
+      const int it = cid + j * ncid;
+      const bool active = it < t_max ? it < t_old : (it == t_max && !stale && n_tree > 0);
+      if (!active) continue;  // uniform across the cluster
+      const int *rows = s_tiles + j * kUM;
+      // ---- main loop ----------------------------------------------------------
+      if (warp == 0 && lane == 0) {  // hidden slices by TMA
+        int issued = 0;
+        for (int kt = 0; kt < nk; ++kt) {
+          const int g = iter * nk + kt, s = g % kSStages;
+          if (g >= kSStages && !mbar_wait(bar_empty + 8 * s, ((g / kSStages) - 1) & 1, u.err)) break;
+          issued = kt + 1;
+          mbar_expect_tx(bar_full + 8 * s, kStageB);
+          tma_load_2d(base + s * kStage + kStageA, &tmH, ((int)crank + kt * kCL) * kUK, 0, bar_full + 8 * s);
+        }
+        // nothing may still be landing in shared memory when the ring is reused
+        const int first = issued > kSStages ? issued - kSStages : 0;
+        for (int kt = first; kt < issued; ++kt) {
+          const int g = iter * nk + kt;
+          mbar_wait(bar_full + 8 * (g % kSStages), (g / kSStages) & 1, u.err);
+        }
+      } else if (warp >= 4) {  // W_head rows by cp.async (rows without an id stay unread)
+        const int p = tid - 128, wl = p >> 5, c = lane & 7;
+        for (int kt = 0; kt < nk; ++kt) {
+          const int g = iter * nk + kt, s = g % kSStages;
+          if (g >= kSStages) mbar_wait(bar_empty + 8 * s, ((g / kSStages) - 1) & 1, u.err);
+          const uint32_t A = base + s * kStage;
+          const int col = ((int)crank + kt * kCL) * kUK + c * 8;
+#pragma unroll
+          for (int rg = 0; rg < kUM / (4 * kGatherWarps); ++rg) {
+            const int row = (rg * kGatherWarps + wl) * 4 + (lane >> 3);
+            const int id = rows[row];
+            if (id >= 0)
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(A + row * 128 + ((c ^ (row & 7)) << 4)),
+                           "l"(u.W + (size_t)id * H + col)
+                           : "memory");
           }
-          s_app[n_draft + lane] = y;
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar_full + 8 * s) : "memory");
         }
-        if (lane == 0) {
-          if (writer && n_ver < K) set_flag(u.err, NS_FLAG_BAD_ID);
-          s_misc[1] = n_draft + n_ver;
+        asm volatile("cp.async.wait_all;" ::: "memory");  // nothing of this thread is still landing
+      } else if (warp == 1 && lane == 0) {
+        bool ok = true;
+        for (int kt = 0; kt < nk && ok; ++kt) {
+          const int g = iter * nk + kt, s = g % kSStages;
+          ok = mbar_wait(bar_full + 8 * s, (g / kSStages) & 1, u.err);
+          if (!ok) break;
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the gathered rows, for the tensor core
+          tc_fence_after();
+          const uint32_t A = base + s * kStage;
+#pragma unroll
+          for (int kk = 0; kk < kUK / 16; ++kk)
+            umma_bf16(tmem, sw128_desc(A + kk * 32), sw128_desc(A + kStageA + kk * 32), (kt | kk) != 0);
+          umma_commit(bar_empty + 8 * s);
         }
+        if (nk > 0 && ok) umma_commit(bar_acc);
+        else mbar_arrive(bar_acc);
       }
-    } else if (tid == 0) {
-      s_misc[1] = s_misc[0];
-    }
-    __syncthreads();
-    const int m = s_misc[1];
-    if (cta == 0 && tid >= kWarp * 2 && tid < kWarp * 2 + m - s_misc[0]) {  // the entering verify ids' rows
-      const int y = s_app[s_misc[0] + tid - kWarp * 2];
-      prefetch_l2(u.W + (size_t)y * u.H, (uint32_t)row_bytes);
-    }
-    // positions: evicted [old_start, old_start + n_ev), appended [ap_begin, len1)
-    const long long len1 = len0 + m;
-    const long long new_start = len1 > W ? len1 - W : 0;
-    const long long ev_end = len0 < new_start ? len0 : new_start;
-    const int n_ev = ev_end > old_start ? (int)(ev_end - old_start) : 0;
-    const long long ap_begin = len0 > new_start ? len0 : new_start;
-    const int n_ap = (int)(len1 - ap_begin);
-    const int ap_off = (int)(ap_begin - len0);
-    if (tid < n_ap) {
-      const int h = hash_insert(h_key, s_app[ap_off + tid]);
-      if (h >= 0) atomicAdd(&h_ap[h], 1);
-    } else if (tid >= kMaxAppendStep && tid < kMaxAppendStep + n_ev) {
-      const int id = s_evid[tid - kMaxAppendStep];
-      const int h = id >= 0 ? hash_find(h_key, id) : -1;
-      if (h >= 0) atomicAdd(&h_ev[h], 1);
-    }
-    __syncthreads();
-    // One thread per distinct id: an appended id is in the window; an evicted
-    // one stays only if it occurs again at a position that is not evicted.
-    int wchg = -1;
-    if (tid < kStepHash) {
-      const int id = h_key[tid];
-      if (id >= 0) {
-        const int ap = h_ap[tid], ev = h_ev[tid];
-        const uint32_t bit = 1u << (id & 31);
-        if (ap > 0) {
-          if (!(s_bits[id >> 5] & bit)) {
-            atomicOr(&s_bits[id >> 5], bit);
-            wchg = id >> 5;
+      __syncwarp();
+      // ---- accumulator -> this CTA's partial tile, then the cluster's sum ----
+      float *Pt = reinterpret_cast<float *>(gbase);  // [64][128], reuses the ring
+      if (warp >= 4 && warp < 8) {  // warp w reads tensor-memory lanes 32 (w % 4) .. + 31
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_acc, iter & 1, u.err));
+        tc_fence_after();
+        const int jj = (warp - 4) * 32 + lane;
+        const uint32_t t0 = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+#pragma unroll
+        for (int c = 0; c < kUN; c += 16) {
+          float v[16];
+          if (nk > 0 && ok) {
+            tmem_ld16(t0 + c, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[q] = 0.f;
           }
-        } else if (ev > 0 && h_last[tid] < n_ev) {
-          atomicAnd(&s_bits[id >> 5], ~bit);
-          wchg = id >> 5;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) Pt[(c + q) * kUM + jj] = v[q];
         }
-        if (writer && ap != ev) atomicAdd(&a.counts[id], (unsigned)(ap - ev));
       }
-    }
-    if (writer) {
-      if (tid < n_ap) a.ring[(head + ap_off + tid) % W] = s_app[ap_off + tid];
-      if (tid == 0) {
-        a.length[0] = len1;
-        a.length[1] = (head + m) % W;
+      tc_fence_before();
+      named_sync(kBarT, kTGroup);
+      if (!cluster_ready) {  // every peer's barriers are initialized
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+        cluster_ready = true;
       }
+      if (ttid == 0) {
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+        for (uint32_t p = 0; p < (uint32_t)kCL; ++p) mbar_arrive_cluster(map_peer(bar_pready, p));
+      }
+      mbar_wait_cluster(bar_pready, iter & 1, u.err);
+      // hidden rows [r0, r0 + nr) summed over the C partials in rank order
+      float *F = Fbuf + j * kFRows * kUM;
+      for (int t = ttid; t < nr * (kUM / 4); t += kTGroup) {
+        const int rr = t / (kUM / 4), c4 = (t % (kUM / 4)) * 4;
+        const uint32_t off = base + (uint32_t)(((r0 + rr) * kUM + c4) * 4);
+        float4 s4 = ld_peer_f4(map_peer(off, 0));
+#pragma unroll
+        for (uint32_t p = 1; p < (uint32_t)kCL; ++p) {
+          const float4 q = ld_peer_f4(map_peer(off, p));
+          s4.x += q.x;
+          s4.y += q.y;
+          s4.z += q.z;
+          s4.w += q.w;
+        }
+        *reinterpret_cast<float4 *>(F + rr * kUM + c4) = s4;
+      }
+      named_sync(kBarT, kTGroup);
+      if (ttid == 0) {
+        for (uint32_t p = 0; p < (uint32_t)kCL; ++p) mbar_arrive_cluster(map_peer(bar_pdone, p));
+      }
+      mbar_wait_cluster(bar_pdone, iter & 1, u.err);  // no peer still reads this CTA's partial
+      ++iter;
     }
-    __syncthreads();
-    if (writer && wchg >= 0) a.bitmap[wchg] = s_bits[wchg];
+    if (!cluster_ready) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (ttid == 0) mbar_arrive(bar_ring);  // the ring is free past the top-k lists
 
-    // compaction: per 4-word group, the number of ids before it (block scan)
-    const int ng = a.nwords_pad / 4;
-    const int G = (ng + kUThreads - 1) / kUThreads;
-    const uint4 *b4 = reinterpret_cast<const uint4 *>(s_bits);
-    int cnt = 0;
-    for (int g = tid * G; g < tid * G + G && g < ng; ++g) {
-      const uint4 w4 = b4[g];
-      cnt += __popc(w4.x) + __popc(w4.y) + __popc(w4.z) + __popc(w4.w);
-    }
-    int total;
-    int off = block_exclusive_scan(cnt, sh_scan, &total);
-    for (int g = tid * G; g < tid * G + G && g < ng; ++g) {
-      s_goff[g] = off;
-      const uint4 w4 = b4[g];
-      off += __popc(w4.x) + __popc(w4.y) + __popc(w4.z) + __popc(w4.w);
-    }
-    m_act = total < W ? total : W;
-    if (writer && tid == 0) {
-      if (total > W) set_flag(u.err, NS_FLAG_OVERFLOW);
-      *a.count = m_act;
-    }
-    __syncthreads();
-    // this CTA's tiles: position p -> the group holding it (the last group
-    // whose offset is <= p), then the word and the bit
-    for (int j = 0; j < tpc; ++j) {
-      const int p = (cid + j * ncid) * kUM + tid;
-      if (tid < kUM && p < m_act) {
-        int lo_g = 0, hi_g = ng - 1;
-        while (lo_g < hi_g) {
-          const int mid = (lo_g + hi_g + 1) >> 1;
-          if (s_goff[mid] <= p) lo_g = mid;
-          else hi_g = mid - 1;
+    // ---- the columns at their positions in I_t ------------------------------
+    const bool okst = mbar_wait(bar_state, 0, u.err);
+    const int m_act = s_misc[3];
+    if (ttid < 2 * kUM && okst) {
+      const int col = ttid & (kUM - 1), rg = ttid / kUM;  // one column per thread, two row groups
+      for (int j = 0; j < nitems; ++j) {
+        const int it = cid + j * ncid;
+        const bool active = it < t_max ? it < t_old : (it == t_max && !stale && n_tree > 0);
+        if (!active) continue;
+        const int id = s_tiles[j * kUM + col];
+        int pos = -1;
+        if (stale) {
+          if (id >= 0 && it * kUM + col < m_act) pos = it * kUM + col;
+        } else if (id >= 0) {
+          const uint32_t w = s_bits[id >> 5], bit = 1u << (id & 31);
+          bool put;
+          if (it < t_max) {
+            put = (w & bit) != 0u;  // stays in the window
+          } else {
+            const int h = hash_find(h_key, id);
+            put = h >= 0 && h_ent[h] != 0 && h_wrow[h] == col;
+          }
+          if (put) {
+            const int g4 = id >> 7;
+            pos = s_goff[g4];
+            for (int q = 4 * g4; q < (id >> 5); ++q) pos += __popc(s_bits[q]);
+            pos += __popc(w & (bit - 1u));
+            if (pos >= m_act) pos = -1;
+          }
         }
-        int r = p - s_goff[lo_g], wi = 4 * lo_g;
-        uint32_t w = s_bits[wi];
-        while (r >= __popc(w)) {
-          r -= __popc(w);
-          w = s_bits[++wi];
+        if (pos >= 0) {
+          const float *F = Fbuf + j * kFRows * kUM;
+          for (int rr = rg; rr < nr; rr += 2)
+            if (r0 + rr < u.n) u.logits[(size_t)(r0 + rr) * u.ld + pos] = F[rr * kUM + col];
         }
-        const int id = wi * 32 + select_bit(w, r);
-        s_tiles[j * kUM + tid] = id;
-        if (tid >= sh0 && tid < sh0 + shn) a.active[p] = id;  // this CTA's share of the tile
       }
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the ring area goes back to the tiles
-    __syncthreads();
+  } else if (vgrp) {
+    // ======================== verify group ====================================
+    // The verify ids that enter the window and are not tree ids: their
+    // logits by CUDA-core dot products, one warp per (id, hidden row) pair;
+    // this CTA takes pairs cta, cta + P, ...
+    const int vw = warp - 2;
+    int npair = 0;
+    const bool okc = mbar_wait(bar_cver, 0, u.err);
+    const int n_draft = s_misc[0], n_ver = okc && !stale ? s_misc[2] : 0;
+    const int n = u.n;
+    for (int i = vw;; i += 2) {
+      const int q = cta + i * P;
+      if (q >= n_ver * n || i >= kVerPairs) break;
+      const int v = q / n, r = q - v * n;
+      const int id = s_app[n_draft + v];
+      const uint4 *wr = reinterpret_cast<const uint4 *>(u.W + (size_t)id * H);
+      const uint4 *hr = reinterpret_cast<const uint4 *>(a.hid + (size_t)r * H);
+      float acc = 0.f;
+      for (int c = lane; c < (H >> 3); c += kWarp) {
+        const uint4 w4 = __ldg(wr + c), h4 = __ldg(hr + c);
+        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w}, hv[4] = {h4.x, h4.y, h4.z, h4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc = fmaf(__uint_as_float(wv[e] << 16), __uint_as_float(hv[e] << 16), acc);
+          acc = fmaf(__uint_as_float(wv[e] & 0xffff0000u), __uint_as_float(hv[e] & 0xffff0000u), acc);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) {
+        s_vdot[i] = acc;
+        s_vpair[i] = q;
+      }
+      ++npair;
+    }
+    __syncwarp();
+    const bool okst = mbar_wait(bar_state, 0, u.err);
+    const int m_act = s_misc[3];
+    if (okst && lane < npair) {  // lane l writes the warp's pair l
+      const int i = vw + 2 * lane, q = s_vpair[i];
+      const int v = q / n, r = q - v * n, id = s_app[n_draft + v];
+      const int h = hash_find(h_key, id);
+      if (h >= 0 && h_ent[h] != 0 && h_wrow[h] == kVerRow0 + v) {
+        const uint32_t w = s_bits[id >> 5], bit = 1u << (id & 31);
+        const int g4 = id >> 7;
+        int pos = s_goff[g4];
+        for (int qq = 4 * g4; qq < (id >> 5); ++qq) pos += __popc(s_bits[qq]);
+        pos += __popc(w & (bit - 1u));
+        if (pos < m_act) u.logits[(size_t)r * u.ld + pos] = s_vdot[i];
+      }
+    }
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   }
 
-  // ---- the tiles --------------------------------------------------------------
-  const int T = (m_act + kUM - 1) / kUM;
-  const int KC = u.H / kUK;
-  const int nk = KC > (int)crank ? (KC - (int)crank + kCL - 1) / kCL : 0;
-  int iter = 0;
-  for (int j = 0; j < tpc; ++j) {
-    const int tile = cid + j * ncid;
-    if (!ok || tile >= T) break;  // uniform across the cluster
-    const int row0 = tile * kUM;
-    if (tid < kUM) S.s_rows[tid] = s_tiles[j * kUM + (row0 + tid < m_act ? tid : m_act - 1 - row0)];
-    __syncthreads();
-    umma_tile<kCL, false, false, false>(S, tmem, tmH, tmP, u, iter, nk, tile, 0, m_act, T);
-    ++iter;
-  }
-
-  // ---- top-k: every CTA ranks whole rows of the logits the tiles wrote ----
-  // (rows cta, cta + P, ...; 8 columns per thread per pass, ties to the
-  // smaller column, which is the smaller id as I_t ascends)
-  if (ok) ok = grid_barrier(a.gbar, (unsigned long long)P, u.err, &s_misc[3]);
-  if (ok) {
-    uint32_t *rk = reinterpret_cast<uint32_t *>(S.gbase);  // [(warps + 1) x K] lists, then the result
-    uint32_t *ri = rk + (kStepWarps + 1) * NS_MAX_TOPK;
-    uint32_t *ok_k = ri + (kStepWarps + 1) * NS_MAX_TOPK, *ok_i = ok_k + NS_MAX_TOPK;
-    const int k = u.k;
-    const bool vec_l = (u.ld % 4 == 0) && (reinterpret_cast<uintptr_t>(u.logits) % 16 == 0);
-    for (int r = cta; r < u.n; r += P) {
-      const float *row = u.logits + (size_t)r * u.ld;
-      if (tid < k) {
-        rk[kStepWarps * k + tid] = 0u;
-        ri[kStepWarps * k + tid] = (uint32_t)kEmptyId;
-      }
-      for (int c0 = 0; c0 < m_act; c0 += 8 * kUThreads) {
-        uint32_t hk[8], hi[8];
-        const int j0 = c0 + 8 * tid;
-        if (vec_l && j0 + 8 <= m_act) {
-          const float4 f0 = __ldcg(reinterpret_cast<const float4 *>(row + j0));
-          const float4 f1 = __ldcg(reinterpret_cast<const float4 *>(row + j0 + 4));
-          const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-#pragma unroll
-          for (int q = 0; q < 8; ++q) hk[q] = order_key(v[q]);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) hk[q] = j0 + q < m_act ? order_key(__ldcg(row + j0 + q)) : 0u;
+  if (!sgrp) {
+    // ---- every CTA's columns are out: rank whole rows ------------------------
+    // (the bitmap and group counts of I_t in this CTA's shared memory map a
+    // column back to its id)
+    const bool ok = grid_barrier(a.gbar, (unsigned long long)P, u.err, &s_flag[2], kBarK, kKThreads, tid == 0) &&
+                    s_misc[3] >= 0;
+    const int m_act = s_misc[3];
+    if (ok) {
+      uint32_t *rk = reinterpret_cast<uint32_t *>(gbase);  // [(warps + 1) x k] lists, then the result
+      uint32_t *ri = rk + (kKWarps + 1) * NS_MAX_TOPK;
+      uint32_t *ok_k = ri + (kKWarps + 1) * NS_MAX_TOPK, *ok_i = ok_k + NS_MAX_TOPK;
+      const int k = u.k;
+      const bool vec_l = (u.ld % 4 == 0) && (reinterpret_cast<uintptr_t>(u.logits) % 16 == 0);
+      for (int r = cta; r < u.n; r += P) {
+        const float *row = u.logits + (size_t)r * u.ld;
+        if (tid < k) {
+          rk[kKWarps * k + tid] = 0u;
+          ri[kKWarps * k + tid] = (uint32_t)kEmptyId;
         }
+        for (int c0 = 0; c0 < m_act; c0 += 8 * kKThreads) {
+          uint32_t hk[8], hi[8];
+          const int j0 = c0 + 8 * tid;
+          if (vec_l && j0 + 8 <= m_act) {
+            const float4 f0 = __ldcg(reinterpret_cast<const float4 *>(row + j0));
+            const float4 f1 = __ldcg(reinterpret_cast<const float4 *>(row + j0 + 4));
+            const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) hi[q] = hk[q] != 0u ? (uint32_t)(j0 + q) : (uint32_t)kEmptyId;
-        uint32_t wk, wi;
-        warp_topk8_lanes(hk, hi, k, &wk, &wi);
-        if (lane < k) {
-          rk[warp * k + lane] = wk;
-          ri[warp * k + lane] = wi;
-        }
-        __syncthreads();
-        if (warp == 0) {
-          uint32_t lk, li;
-          warp_merge_lists(rk, ri, kStepWarps + 1, k, ok_k, ok_i, lk, li);
+            for (int q = 0; q < 8; ++q) hk[q] = order_key(v[q]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) hk[q] = j0 + q < m_act ? order_key(__ldcg(row + j0 + q)) : 0u;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) hi[q] = hk[q] != 0u ? (uint32_t)(j0 + q) : (uint32_t)kEmptyId;
+          uint32_t wk, wi;
+          warp_topk8_lanes(hk, hi, k, &wk, &wi);
           if (lane < k) {
-            rk[kStepWarps * k + lane] = ok_k[lane];
-            ri[kStepWarps * k + lane] = ok_i[lane];
+            rk[warp * k + lane] = wk;
+            ri[warp * k + lane] = wi;
+          }
+          named_sync(kBarK, kKThreads);
+          if (warp == 0) {
+            uint32_t lk, li;
+            warp_merge_lists(rk, ri, kKWarps + 1, k, ok_k, ok_i, lk, li);
+            if (lane < k) {
+              rk[kKWarps * k + lane] = ok_k[lane];
+              ri[kKWarps * k + lane] = ok_i[lane];
+            }
+          }
+          named_sync(kBarK, kKThreads);
+        }
+        if (tid < k) {  // column -> id through I_t
+          const uint32_t key = rk[kKWarps * k + tid];
+          const int jc = (int)ri[kKWarps * k + tid];
+          u.out_ids[r * k + tid] = key != 0u ? nth_id(s_bits, s_goff, a.nwords_pad / 4, jc) : -1;
+          u.out_vals[r * k + tid] = key != 0u ? key_value(key) : -__int_as_float(0x7f800000);
+        }
+        named_sync(kBarK, kKThreads);
+      }
+    }
+  } else {
+    // ======================== state group =====================================
+    const int swarp = stid >> 5;
+    for (int q = stid; q < kStepHash; q += kSgThreads) {
+      h_key[q] = -1;
+      h_cnt[q] = 0;
+      h_ev[q] = 0;
+      h_ap[q] = 0;
+      h_wrow[q] = 0x7fffffff;
+      h_ent[q] = 0;
+      h_chg[q] = -1;
+    }
+    if (stid < n_tree) s_tree[stid] = tree_id;
+    // the old window: |S|, its ring slot, the entries that may leave and
+    // their counts in the window
+    if (!mbar_wait(sbar, 0, u.err)) s_flag[1] = 1;
+    named_sync(kBarS, kSgThreads);
+    const bool have = s_flag[1] == 0;
+    const long long len0 = s_len[0];
+    const int head = (int)s_len[1];
+    const long long old_start = len0 > W ? len0 - W : 0;
+    const int n_old = (int)(len0 - old_start);
+    int max_ev = n_tree + K;
+    if (max_ev > n_old) max_ev = n_old;
+    int ev_id = -1;
+    uint32_t ev_cnt = 0u;
+    if (stid < max_ev) {  // position old_start + stid
+      const int slot = len0 > W ? (head + stid >= W ? head + stid - W : head + stid) : stid;
+      ev_id = s_ring[slot];
+      if ((unsigned)ev_id >= (unsigned)V) {  // the ring only ever holds valid ids
+        if (writer) set_flag(u.err, NS_FLAG_INTERNAL | (2u << 8));
+        ev_id = -1;
+      }
+      if (ev_id >= 0) ev_cnt = __ldcg(a.counts + ev_id);  // read before the grid barrier, used after it
+      s_evid[stid] = ev_id;
+    }
+
+    // C_draft: distinct valid tree ids in first-occurrence node order, with
+    // the tree row of each (state warp 0)
+    if (swarp == 0) {
+      const int ta = lane < n_tree ? s_tree[lane] : 0;
+      const int tb = lane + 32 < n_tree ? s_tree[lane + 32] : 0;
+      const bool va = lane < n_tree && (unsigned)ta < (unsigned)V;
+      const bool vb = lane + 32 < n_tree && (unsigned)tb < (unsigned)V;
+      if (writer && ((lane < n_tree && !va) || (lane + 32 < n_tree && !vb))) set_flag(u.err, NS_FLAG_BAD_ID);
+      const int ka = va ? ta : -1 - lane, kb = vb ? tb : -33 - lane;
+      const unsigned ma = __match_any_sync(0xffffffffu, ka);
+      const unsigned mb = __match_any_sync(0xffffffffu, kb);
+      bool in_a = false;
+#pragma unroll 4
+      for (int q = 0; q < kWarp; ++q) in_a |= __shfl_sync(0xffffffffu, ka, q) == kb;
+      const bool keep_a = va && __ffs(ma) - 1 == lane;
+      const bool keep_b = vb && __ffs(mb) - 1 == lane && !in_a;
+      const unsigned ba = __ballot_sync(0xffffffffu, keep_a), bb = __ballot_sync(0xffffffffu, keep_b);
+      const unsigned lt = (1u << lane) - 1u;
+      if (keep_a) {
+        s_app[__popc(ba & lt)] = ta;
+        s_arow[__popc(ba & lt)] = lane;
+      }
+      if (keep_b) {
+        s_app[__popc(ba) + __popc(bb & lt)] = tb;
+        s_arow[__popc(ba) + __popc(bb & lt)] = lane + 32;
+      }
+      if (lane == 0) s_misc[0] = __popc(ba) + __popc(bb);
+    }
+
+    // the slice's Top-K: per pass of eight values per thread, each warp's K
+    // best, then state warp 0 merges the warps' lists with the running one
+    if (stid < K) {
+      wl_k[kSgWarps * K + stid] = 0u;  // the running Top-K starts empty
+      wl_i[kSgWarps * K + stid] = (uint32_t)kEmptyId;
+    }
+    for (int c0 = 0; c0 < nsl; c0 += kPass) {
+      if (c0 > 0) load_pass(c0);
+      uint32_t hk[8], hi[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int e = a.vec ? 4 * ((q >> 2) * kSgThreads + stid) + (q & 3) : q * kSgThreads + stid;
+        hk[q] = order_key(x[q]);  // padding is NaN: key 0, never ranks
+        hi[q] = hk[q] != 0u ? (uint32_t)(lo + c0 + e) : (uint32_t)kEmptyId;
+      }
+      uint32_t wk, wi;
+      warp_topk8_lanes(hk, hi, K, &wk, &wi);
+      if (lane < K) {
+        wl_k[swarp * K + lane] = wk;
+        wl_i[swarp * K + lane] = wi;
+      }
+      named_sync(kBarS, kSgThreads);
+      if (swarp == 0) {
+        uint32_t lk, li;
+        warp_merge_lists(wl_k, wl_i, kSgWarps + 1, K, res_k, res_i, lk, li);
+        if (lane < K) {
+          wl_k[kSgWarps * K + lane] = res_k[lane];
+          wl_i[kSgWarps * K + lane] = res_i[lane];
+        }
+      }
+      named_sync(kBarS, kSgThreads);
+    }
+    if (stid < K) {
+      a.vk[cta * K + stid] = wl_k[kSgWarps * K + stid];
+      a.vi[cta * K + stid] = wl_i[kSgWarps * K + stid];
+    }
+    if (ev_id >= 0) {  // the evictable ids and their window counts
+      const int h = hash_insert(h_key, ev_id);
+      if (h >= 0) h_cnt[h] = (int)ev_cnt;  // every occurrence of an id read the same count
+    }
+
+    // ---- grid barrier: every CTA's Top-K is out, every old-state read done --
+    if (stid == 0 && !mbar_wait(bar_old, 0, u.err)) s_flag[1] = 1;
+    const bool ok = grid_barrier(a.gbar, (unsigned long long)P, u.err, &s_flag[3], kBarS, kSgThreads, stid == 0) &&
+                    have && s_flag[1] == 0;
+
+    // ---- C_ver, the window update, I_t --------------------------------------
+    int m_act = 0;
+    if (ok) {
+      for (int q = stid; q < P * K; q += kSgThreads) {
+        s_vk[q] = __ldcg(a.vk + q);
+        s_vi[q] = __ldcg(a.vi + q);
+      }
+      named_sync(kBarS, kSgThreads);
+      if (K > 0) {  // two rounds of list merging: 4 groups of at most 64 lists, then the 4 results
+        const int per_warp = (P + kSgWarps - 1) / kSgWarps;
+        const int l0 = swarp * per_warp;
+        const int nl = P - l0 < per_warp ? (P - l0 > 0 ? P - l0 : 0) : per_warp;
+        warp_merge_lists64(s_vk + l0 * K, s_vi + l0 * K, nl, K, wl_k + swarp * K, wl_i + swarp * K);
+        named_sync(kBarS, kSgThreads);
+        if (swarp == 0) {
+          uint32_t lk, li;
+          warp_merge_lists(wl_k, wl_i, kSgWarps, K, res_k, res_i, lk, li);
+          const int n_draft = s_misc[0];
+          const bool got = lane < K && res_k[lane] != 0u;
+          const int n_ver = __popc(__ballot_sync(0xffffffffu, got));
+          if (got) {
+            int y = (int)res_i[lane];
+            if ((unsigned)y >= (unsigned)V) {  // cannot happen for a well-formed merge
+              if (writer) set_flag(u.err, NS_FLAG_INTERNAL | (1u << 8));
+              y = 0;
+            }
+            s_app[n_draft + lane] = y;
+            s_arow[n_draft + lane] = kVerRow0 + lane;
+          }
+          if (lane == 0) {
+            if (writer && n_ver < K) set_flag(u.err, NS_FLAG_BAD_ID);
+            s_misc[1] = n_draft + n_ver;
+            s_misc[2] = n_ver;
           }
         }
-        __syncthreads();
+      } else if (stid == 0) {
+        s_misc[1] = s_misc[0];
+        s_misc[2] = 0;
       }
-      if (tid < k) {  // column -> id through I_t
-        const uint32_t key = rk[kStepWarps * k + tid];
-        const int j = (int)ri[kStepWarps * k + tid];
-        u.out_ids[r * k + tid] = key != 0u ? __ldcg(a.active + j) : -1;
-        u.out_vals[r * k + tid] = key != 0u ? key_value(key) : -__int_as_float(0x7f800000);
+      named_sync(kBarS, kSgThreads);
+      if (stid == 0) mbar_arrive(bar_cver);  // the verify group may take its products
+      const int m = s_misc[1];
+      // positions: evicted [old_start, old_start + n_ev), appended [ap_begin, len1)
+      const long long len1 = len0 + m;
+      const long long new_start = len1 > W ? len1 - W : 0;
+      const long long ev_end = len0 < new_start ? len0 : new_start;
+      const int n_ev = ev_end > old_start ? (int)(ev_end - old_start) : 0;
+      const long long ap_begin = len0 > new_start ? len0 : new_start;
+      const int n_ap = (int)(len1 - ap_begin);
+      const int ap_off = (int)(ap_begin - len0);
+      if (stid < n_ap) {
+        const int h = hash_insert(h_key, s_app[ap_off + stid]);
+        if (h >= 0) {
+          atomicAdd(&h_ap[h], 1);
+          atomicMin(&h_wrow[h], s_arow[ap_off + stid]);
+        }
       }
-      __syncthreads();
+      for (int q = stid; q < n_ev; q += kSgThreads) {
+        const int id = s_evid[q];
+        const int h = id >= 0 ? hash_find(h_key, id) : -1;
+        if (h >= 0) atomicAdd(&h_ev[h], 1);
+      }
+      named_sync(kBarS, kSgThreads);
+      // One thread per distinct id: an appended id is in the window (it
+      // enters if its bit was clear); an evicted one leaves when its count
+      // in the window drops to zero.
+      for (int q = stid; q < kStepHash; q += kSgThreads) {
+        const int id = h_key[q];
+        if (id >= 0) {
+          const int ap = h_ap[q], ev = h_ev[q];
+          const uint32_t bit = 1u << (id & 31);
+          if (ap > 0) {
+            if (!(s_bits[id >> 5] & bit)) {
+              atomicOr(&s_bits[id >> 5], bit);
+              h_ent[q] = 1;
+              h_chg[q] = id >> 5;
+            }
+          } else if (ev > 0) {
+            const int now = h_cnt[q] - ev;
+            if (now < 0 && writer) set_flag(u.err, NS_FLAG_OVERFLOW);
+            if (now <= 0) {
+              atomicAnd(&s_bits[id >> 5], ~bit);
+              h_chg[q] = id >> 5;
+            }
+          }
+          if (writer && ap != ev) atomicAdd(&a.counts[id], (unsigned)(ap - ev));
+        }
+      }
+      if (writer) {
+        if (stid < n_ap) a.ring[(head + ap_off + stid) % W] = s_app[ap_off + stid];
+        if (stid == 0) {
+          a.length[0] = len1;
+          a.length[1] = (head + m) % W;
+          *a.active_len = len1;
+        }
+      }
+      named_sync(kBarS, kSgThreads);
+      if (writer) {
+        for (int q = stid; q < kStepHash; q += kSgThreads)
+          if (h_chg[q] >= 0) a.bitmap[h_chg[q]] = s_bits[h_chg[q]];
+      }
+
+      // compaction: per 4-word group, the number of ids before it
+      const int ng = a.nwords_pad / 4;
+      const int G = (ng + kSgThreads - 1) / kSgThreads;
+      const uint4 *b4 = reinterpret_cast<const uint4 *>(s_bits);
+      int cnt = 0;
+      for (int g = stid * G; g < stid * G + G && g < ng; ++g) {
+        const uint4 w4 = b4[g];
+        cnt += __popc(w4.x) + __popc(w4.y) + __popc(w4.z) + __popc(w4.w);
+      }
+      int total;
+      int off = sg_exclusive_scan(cnt, sh_scan, &total);
+      for (int g = stid * G; g < stid * G + G && g < ng; ++g) {
+        s_goff[g] = off;
+        const uint4 w4 = b4[g];
+        off += __popc(w4.x) + __popc(w4.y) + __popc(w4.z) + __popc(w4.w);
+      }
+      m_act = total < W ? total : W;
+      if (stid == 0) s_misc[3] = m_act;
+      if (writer && stid == 0) {
+        if (total > W) set_flag(u.err, NS_FLAG_OVERFLOW);
+        *a.count = m_act;
+      }
+      named_sync(kBarS, kSgThreads);
+      if (stid == 0) mbar_arrive(bar_state);  // the tile and verify groups may place their columns
+      // this CTA's share of I_t: positions [p0, p0 + share)
+      const int share = share_of(W, P), p0 = cta * share;
+      for (int i = stid; i < share; i += kSgThreads) {
+        const int p = p0 + i;
+        int id = -1;
+        if (p < m_act) {
+          id = nth_id(s_bits, s_goff, ng, p);
+          a.active[p] = id;
+        }
+        s_share[i] = id;
+      }
+    } else if (stid == 0) {
+      s_misc[3] = -1;  // no columns, no ranking
+      mbar_arrive(bar_cver);
+      mbar_arrive(bar_state);
     }
+    named_sync(kBarS, kSgThreads);
+    // ---- the packed buffer: the rows of this CTA's share by bulk copies
+    // through the stage ring (once the tile group is done with it), beside
+    // the top-k
+    if (ok && stid == 0) {
+      const int share = share_of(W, P), p0 = cta * share;
+      int nsh = m_act - p0;
+      if (nsh > share) nsh = share;
+      const uint32_t rb = (uint32_t)H * 2u;  // row bytes (a multiple of 16)
+      const int nbuf = (int)((kSRing - kCopyOff) / rb);
+      if (nsh > 0 && nbuf > 0 && mbar_wait(bar_ring, 0, u.err)) {
+        const uint32_t stage = base + kCopyOff;
+        int phase = 0;
+        for (int i0 = 0; i0 < nsh; i0 += nbuf, ++phase) {
+          const int nb = nsh - i0 < nbuf ? nsh - i0 : nbuf;
+          mbar_expect_tx(bar_copy, (uint32_t)nb * rb);
+          for (int b = 0; b < nb; ++b) bulk_load(stage + b * rb, u.W + (size_t)s_share[i0 + b] * H, rb, bar_copy);
+          if (!mbar_wait(bar_copy, phase & 1, u.err)) break;
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          for (int b = 0; b < nb; ++b)
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                             a.packed + (size_t)(p0 + i0 + b) * H),
+                         "r"(stage + b * rb), "r"(rb)
+                         : "memory");
+          bulk_commit();
+          bulk_wait_read_all();  // the staging may be refilled
+        }
+        bulk_wait_all();
+      }
+    }
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   }
-  if (warp == 2 && lane == 0) bulk_wait_all();  // the packed-buffer stores are complete before the CTA leaves
+  tc_fence_before();
+  __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
@@ -620,15 +1059,15 @@ int g_step_clusters[kNumStepSizes] = {0, 0, 0, 0};  // resident clusters of each
 
 template <int CL>
 int prepare_one() {
-  cudaError_t e = cudaFuncSetAttribute(step_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
+  cudaError_t e = cudaFuncSetAttribute(step_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL, 1, 1);
-  cfg.blockDim = dim3(kUThreads, 1, 1);
-  cfg.dynamicSmemBytes = kUSmem;
+  cfg.blockDim = dim3(kSThreads, 1, 1);
+  cfg.dynamicSmemBytes = kMaxSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
@@ -654,22 +1093,26 @@ cudaError_t prepare_step_kernel() {
   return cudaSuccess;
 }
 
-// The grid must be resident at once (its CTAs wait for each other), so it
-// has at most the resident clusters, which then run several tiles each.
-// Take the cluster size with the fewest tiles per cluster, then the largest
-// (a smaller share of H per CTA).
+// The grid must be resident at once (its CTAs wait for each other).  Its work
+// items are the tiles of W_max rows plus the draft item; take
+// the cluster size that runs them with the fewest items per cluster, then the
+// largest (a smaller share of H per CTA), and just enough clusters.
 int step_plan(const Dims &d, int *tiles_per_cluster, int *cluster_size) {
-  const int tiles = (d.W_max + kUM - 1) / kUM;
+  const int items = (d.W_max + kUM - 1) / kUM + 1;
   int best_ncl = 0, best_tpc = 0, best_size = 0;
   for (int i = 0; i < kNumStepSizes; ++i) {
     const int size = kStepSizes[i];
-    int ncl = g_step_clusters[i] < kMaxStepCtas / size ? g_step_clusters[i] : kMaxStepCtas / size;
-    if (ncl > tiles) ncl = tiles;
-    if (ncl < 1) continue;
-    const int tpc = (tiles + ncl - 1) / ncl;
-    if (tpc > kMaxTilesPerCluster) continue;
-    const StepSmem L = step_smem(d.nwords_pad, (d.W_max + 3) & ~3, ncl * size, d.K_ver);
-    if ((size_t)L.total * 4 > (size_t)kRingBytes) continue;
+    const int most = g_step_clusters[i] < kMaxStepCtas / size ? g_step_clusters[i] : kMaxStepCtas / size;
+    if (most < 1) continue;
+    const int tpc = (items + most - 1) / most;
+    if (tpc > kMaxItemsPerCluster) continue;
+    int ncl = (items + tpc - 1) / tpc;
+    // enough CTAs for the verify products (kVerPairs per CTA)
+    const int pairs = d.K_ver * NS_MAX_ROWS, ctas = (pairs + kVerPairs - 1) / kVerPairs;
+    if (ncl * size < ctas) ncl = (ctas + size - 1) / size;
+    if (ncl > most) continue;
+    const StepSmem L = step_smem(d.nwords_pad, (d.W_max + 3) & ~3, d.W_max, ncl * size, d.K_ver);
+    if (step_smem_bytes(L) > kMaxSmem) continue;
     if (best_ncl == 0 || tpc < best_tpc) {
       best_ncl = ncl;
       best_tpc = tpc;
@@ -682,16 +1125,12 @@ int step_plan(const Dims &d, int *tiles_per_cluster, int *cluster_size) {
 }
 
 cudaError_t launch_step(const StepLaunch &L, cudaStream_t st) {
-  CUtensorMap tmH, tmP;
-  if (!L.probe && (!encode_bf16_2d(&tmH, L.hid, L.d.H, L.n, kUK, kUN) ||
-                   !encode_bf16_2d(&tmP, L.s.packed, L.d.H, L.d.W_max, kUK, kUM)))
-    return cudaErrorInvalidValue;
-  if (L.probe) memset(&tmH, 0, sizeof(tmH)), memset(&tmP, 0, sizeof(tmP));
+  CUtensorMap tmH;
+  if (!L.probe && !encode_bf16_2d(&tmH, L.hid, L.d.H, L.n, kUK, kUN)) return cudaErrorInvalidValue;
+  if (L.probe) memset(&tmH, 0, sizeof(tmH));
   StepArgs a{};
   UmmaArgs &u = a.u;
   u.W = L.W;
-  u.idx = L.s.active;
-  u.count_ptr = L.s.count;
   u.V = L.d.V;
   u.H = L.d.H;
   u.n = L.n;
@@ -699,20 +1138,18 @@ cudaError_t launch_step(const StepLaunch &L, cudaStream_t st) {
   u.W_max = L.d.W_max;
   u.logits = L.logits;
   u.ld = L.ld;
-  u.cand_k = L.s.cand_k;
-  u.cand_i = L.s.cand_i;
-  u.slice_ticket = L.s.slice_ticket;
   u.out_ids = L.out_ids;
   u.out_vals = L.out_vals;
   u.err = L.err;
-  u.nseq = 1;
-  u.tiles_per_seq = (L.d.W_max + kUM - 1) / kUM;
   a.ring = L.s.ring;
   a.counts = L.s.counts;
   a.bitmap = L.s.bitmap;
   a.active = L.s.active;
   a.count = L.s.count;
   a.length = L.s.length;
+  a.active_len = L.s.active_len;
+  a.packed = L.s.packed;
+  a.hid = L.hid;
   a.gbar = L.s.gbar;
   a.vk = L.s.vcand_k;
   a.vi = L.s.vcand_i;
@@ -722,24 +1159,27 @@ cudaError_t launch_step(const StepLaunch &L, cudaStream_t st) {
   a.K = L.d.K_ver;
   a.nwords_pad = L.d.nwords_pad;
   a.ring_words = (L.d.W_max + 3) & ~3;
-  a.tiles_per_cluster = L.tiles_per_cluster;
+  a.items_per_cluster = L.tiles_per_cluster;
+  a.t_max = (L.d.W_max + kUM - 1) / kUM;
   a.vec = L.d.K_ver > 0 && (L.d.V % 4 == 0) && (reinterpret_cast<uintptr_t>(L.zrow) % 16 == 0);
   a.probe = L.probe ? 1 : 0;
+  const int P = L.clusters * L.cluster_size;
+  const StepSmem S = step_smem(L.d.nwords_pad, a.ring_words, L.d.W_max, P, L.d.K_ver);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(L.clusters * L.cluster_size));
-  cfg.blockDim = dim3(kUThreads);
-  cfg.dynamicSmemBytes = kUSmem;
+  cfg.gridDim = dim3((unsigned)P);
+  cfg.blockDim = dim3(kSThreads);
+  cfg.dynamicSmemBytes = (size_t)step_smem_bytes(S);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA waits for every other at the grid barrier
+  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA waits for every other at the grid barriers
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   switch (L.cluster_size) {
-    case 8: return cudaLaunchKernelEx(&cfg, step_kernel<8>, tmH, tmP, a);
-    case 6: return cudaLaunchKernelEx(&cfg, step_kernel<6>, tmH, tmP, a);
-    case 5: return cudaLaunchKernelEx(&cfg, step_kernel<5>, tmH, tmP, a);
-    case 4: return cudaLaunchKernelEx(&cfg, step_kernel<4>, tmH, tmP, a);
+    case 8: return cudaLaunchKernelEx(&cfg, step_kernel<8>, tmH, a);
+    case 6: return cudaLaunchKernelEx(&cfg, step_kernel<6>, tmH, a);
+    case 5: return cudaLaunchKernelEx(&cfg, step_kernel<5>, tmH, a);
+    case 4: return cudaLaunchKernelEx(&cfg, step_kernel<4>, tmH, a);
     default: return cudaErrorInvalidValue;
   }
 }
