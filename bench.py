@@ -37,7 +37,7 @@ if ROOT not in sys.path:
 METRIC = "draft sub-LM-head steps/sec and us/step at V=128k,H=4096,|I_t|~3k; % HBM roofline"
 DEFAULT_WORKLOAD = "llama3_8b_v128256_h4096"
 FLUSH_BYTES = 256 << 20
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gather_project_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
 
 
 # ---------------------------------------------------------------------------

@@ -62,6 +62,7 @@ constexpr int kKWarps = kKThreads / kWarp;
 constexpr int kBarT = 1, kBarS = 2, kBarK = 3;        // named barriers of the groups
 constexpr int kVerPairs = 16;                         // most (verify id, hidden row) products of one CTA
 constexpr int kCopyOff = 8192;                        // packed-copy staging in the ring, past the top-k lists
+constexpr int kMinStepCtas = 120;                     // grid the state update wants (slices of the verify row)
 constexpr int kSStages = 6;                           // stage ring of the tiles
 constexpr int kSRing = kSStages * kStage;
 constexpr int kMaxItemsPerCluster = 2;
@@ -1111,6 +1112,10 @@ int step_plan(const Dims &d, int *tiles_per_cluster, int *cluster_size) {
     const int pairs = d.K_ver * NS_MAX_ROWS, ctas = (pairs + kVerPairs - 1) / kVerPairs;
     if (ncl * size < ctas) ncl = (ctas + size - 1) / size;
     if (ncl > most) continue;
+    // the state update runs on every CTA (the verify row in slices): take
+    // about as many CTAs as a full window would, where they are resident
+    const int want = (kMinStepCtas + size - 1) / size;
+    if (ncl < want) ncl = want < most ? want : most;
     const StepSmem L = step_smem(d.nwords_pad, (d.W_max + 3) & ~3, d.W_max, ncl * size, d.K_ver);
     if (step_smem_bytes(L) > kMaxSmem) continue;
     if (best_ncl == 0 || tpc < best_tpc) {
