@@ -188,9 +188,14 @@ NS_API ns_status ns_sub_lm_head_logits_topk(ns_handle *h, int32_t seq, const uin
  * packed buffer) and the projection with top-k, with the same arguments and
  * results as those calls made in order on `stream`.  Where the device holds
  * the whole grid at once it is ONE cooperative launch (ns_step_launches
- * returns 1): every CTA ranks a slice of the verify row, one grid barrier
- * joins them, and each CTA then updates the window and compacts I_t for its
- * own tiles before running them; otherwise it is ns_state_update followed by
+ * returns 1): while some warps of every CTA update the window (a slice of
+ * the verify row each, a grid barrier, the merge, append, evict, compact),
+ * the others already project the rows of I_{t-1} and of the tree ids, and
+ * each column is written at its id's position once I_t is known; a second
+ * grid barrier precedes the per-row top-k.  When the window changed since
+ * I_t was last built (ns_stream_init or ns_stream_append without
+ * ns_build_active_vocab) the same launch projects I_t after computing it
+ * (same results, slower).  Otherwise it is ns_state_update followed by
  * ns_gather_sub_lm_head_topk.
  */
 NS_API ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
