@@ -369,9 +369,12 @@ NS_API ns_status ns_trace_events(ns_handle *h, ns_event *events, int32_t n_event
  * Dense head on a fixed row range: logits over rows [0, rows) of W_head
  * (rows = V is the full-vocabulary LM head of Eq. 1; rows = 32768 a static
  * frequency-ranked sub-head) and per-row top-k with ids = row numbers.
- * Uses the handle's dense scratch (sized for V rows); the handle's V and H
- * bound `rows` and fix H.  Arguments as in ns_sub_lm_head_logits_topk;
- * ld_logits >= rows when d_logits is not NULL.
+ * Three launches: the projection on the tensor cores (whole 128-row tiles
+ * of W_head by TMA, one persistent CTA per SM), then the top-k of 4096-column
+ * slices of every row and their merge.  Uses the handle's dense scratch
+ * (sized for V rows); the handle's V and H bound `rows` and fix H.
+ * Arguments as in ns_sub_lm_head_logits_topk; ld_logits >= rows when
+ * d_logits is not NULL.
  */
 NS_API ns_status ns_dense_lm_head_topk(ns_handle *h, const uint16_t *d_W_head, int32_t rows,
                                 const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits,
@@ -388,12 +391,12 @@ NS_API ns_status ns_dense_lm_head_topk(ns_handle *h, const uint16_t *d_W_head, i
  * instead of through a handle: logits over rows [0, rows) of W_head (bf16
  * [rows x H], 64 <= H <= 8192, H % 64 == 0) and per-row top-k with ids = row
  * numbers.  It calls no cudaMalloc/cudaFree and no allocating library
- * routine.  Its scratch is a fixed array of 6,817,792 bytes (6.5 MiB) inside
+ * routine.  Its scratch is a fixed array of 6,291,456 bytes (6 MiB) inside
  * the library image, reserved on every GPU that loads the library until the
- * process exits.  It runs one CTA per SM where ns_dense_lm_head_topk runs
- * two, so it is slower on large heads, and it splits the sum over H
- * differently: the logits agree with the handle's to fp32 rounding, not bit
- * for bit.  `stream` must belong to the current device (NS_ERR_ARG
+ * process exits.  It runs the same kernels as ns_dense_lm_head_topk, so the
+ * logits and top-k are the handle's, bit for bit.  rows <= 2^19.  A bounded
+ * wait that runs out is recorded in a word of the library image that no call
+ * reads back.  `stream` must belong to the current device (NS_ERR_ARG
  * otherwise).  When d_logits is NULL the logits are kept in that scratch, which
  * holds at most NS_NOALLOC_MAX_LOGITS values: n * rows above that returns
  * NS_ERR_ARG (pass d_logits for larger heads, e.g. the full vocabulary).

@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libnanospec.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
-SOURCES = ["ns_api.cu", "ns_state.cu", "ns_project.cu", "ns_noalloc.cu", "ns_umma.cu", "ns_slots.cu", "ns_step.cu"]
+SOURCES = ["ns_api.cu", "ns_state.cu", "ns_topk.cu", "ns_noalloc.cu", "ns_umma.cu", "ns_slots.cu", "ns_step.cu",
+           "ns_dense.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH_FLAGS + [
     "-O3",

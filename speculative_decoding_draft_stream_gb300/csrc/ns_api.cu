@@ -17,7 +17,6 @@ struct ns_handle {
   ns::Dims dims;
   int device = 0;
   int num_sms = 0;
-  int pgrid = 1;  // CTAs of the projection
   int ggrid = 1;  // CTAs of the gather
   int sgrid = 1;  // CTAs of the slot-row copy
   char *base = nullptr;
@@ -26,8 +25,8 @@ struct ns_handle {
   std::vector<ns::SeqDev> seqs;
   std::vector<char> inited;
   float *dense_logits = nullptr;  // [kProjBN x dense_ld]
-  float *dense_part = nullptr;    // [pgrid x tile]
-  int32_t *dense_tickets = nullptr;
+  uint32_t *dense_cand_k = nullptr;  // [NS_MAX_ROWS x topk slices of V x NS_MAX_TOPK] slices' top-k lists
+  uint32_t *dense_cand_i = nullptr;
   int dense_ld = 0;
   int step_clusters = 0;  // clusters of the one-launch step (0: two launches)
   int step_tpc = 0;       // tiles per cluster of the one-launch step
@@ -118,8 +117,9 @@ void layout(ns_handle *h, Carver &cv) {
   }
   h->dense_ld = (c.V + 3) & ~3;
   h->dense_logits = cv.take<float>((size_t)ns::kProjBN * h->dense_ld);
-  h->dense_part = cv.take<float>((size_t)h->pgrid * ns::kProjBN * ns::kProjBM);
-  h->dense_tickets = cv.take<int32_t>(h->pgrid);
+  const size_t ncand = (size_t)NS_MAX_ROWS * ns::topk_slices(c.V) * NS_MAX_TOPK;
+  h->dense_cand_k = cv.take<uint32_t>(ncand);
+  h->dense_cand_i = cv.take<uint32_t>(ncand);
 }
 
 bool valid_seq(const ns_handle *h, int32_t seq) { return h && seq >= 0 && seq < h->cfg.batch; }
@@ -156,8 +156,8 @@ ns_status ns_create(const ns_config *cfg, ns_handle **out) {
   h->cfg = c;
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
-      ns::prepare_project_kernels() != cudaSuccess || ns::prepare_umma_kernels() != cudaSuccess ||
-      ns::prepare_step_kernel() != cudaSuccess) {
+      ns::prepare_umma_kernels() != cudaSuccess ||
+      ns::prepare_step_kernel() != cudaSuccess || ns::prepare_dense_kernel() != cudaSuccess) {
     delete h;
     return NS_ERR_CUDA;
   }
@@ -174,7 +174,6 @@ ns_status ns_create(const ns_config *cfg, ns_handle **out) {
     delete h;
     return NS_ERR_CUDA;
   }
-  h->pgrid = 2 * h->num_sms;
   h->ggrid = 4 * h->num_sms;
   h->sgrid = 2 * h->num_sms;
 
@@ -658,18 +657,11 @@ ns_status ns_dense_lm_head_topk(ns_handle *h, const uint16_t *d_W_head, int32_t 
   ns_status st = check_proj_args(h, d_hidden, n, k, d_logits, ld_logits, rows, d_topk_ids, d_topk_vals);
   if (st != NS_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  ns::ProjArgs a{};
-  a.rows = d_W_head;
-  a.rows_host = rows;
-  a.hid = d_hidden;
-  a.n = n;
-  a.H = h->cfg.H;
-  a.logits = d_logits ? d_logits : h->dense_logits;
-  a.ld = d_logits ? ld_logits : h->dense_ld;
-  a.part = h->dense_part;
-  a.tickets = h->dense_tickets;
-  cudaError_t e = ns::launch_project(a, h->pgrid, cs);
-  if (e == cudaSuccess) e = ns::launch_topk(a.logits, a.ld, nullptr, rows, nullptr, n, k, d_topk_ids, d_topk_vals, cs);
+  float *logits = d_logits ? d_logits : h->dense_logits;
+  const int ld = d_logits ? ld_logits : h->dense_ld;
+  cudaError_t e = ns::launch_dense(d_W_head, rows, d_hidden, n, h->cfg.H, logits, ld, h->err, cs);
+  if (e == cudaSuccess)
+    e = ns::launch_topk(logits, ld, rows, nullptr, n, k, d_topk_ids, d_topk_vals, h->dense_cand_k, h->dense_cand_i, cs);
   return cuda_status(e);
 }
 

@@ -12,12 +12,7 @@
 namespace ns {
 
 constexpr int kWarp = 32;
-constexpr int kProjBM = 64;      // W_head rows per projection tile
-constexpr int kProjBN = 64;      // hidden rows per tile (NS_MAX_ROWS)
-constexpr int kProjBK = 64;      // k per pipeline stage (128 bytes of a bf16 row)
-constexpr int kProjStages = 4;   // cp.async pipeline depth
-constexpr int kProjThreads = 128;
-constexpr int kProjMaxSplit = 16;  // most K-splits of one row tile
+constexpr int kProjBN = 64;      // hidden rows of a projection (NS_MAX_ROWS): rows of the logits scratch
 constexpr int kStateThreads = 1024;
 constexpr int kTopkThreads = 256;
 constexpr int kInitTopkThreads = 256;
@@ -450,24 +445,20 @@ cudaError_t prepare_slot_kernels(const Dims &d);
 cudaError_t launch_slot_update(const SeqDev &s, const Dims &d, const uint16_t *W, int copy_grid, uint32_t *err,
                                cudaStream_t st);
 
-// Dense head (ns_project.cu): rows [0, rows_host) of W_head.
-struct ProjArgs {
-  const uint16_t *rows;      // W_head
-  int32_t rows_host;         // row count
-  const uint16_t *hid;       // [n x H]
-  int32_t n, H;
-  float *logits;             // [n x ld]
-  int32_t ld;
-  float *part;               // split-K partial tiles
-  int32_t *tickets;          // per-tile arrival counters
-};
+// Per-row top-k of a dense head's logits (ns_topk.cu): two launches, the
+// slices' lists (order keys and columns) in cand_k/cand_i, n x
+// topk_slices(rows) x k entries each; at most 128 slices.
+constexpr int kTopkSliceCols = 4096;
+__host__ __device__ inline int topk_slices(int rows) { return (rows + kTopkSliceCols - 1) / kTopkSliceCols; }
+cudaError_t launch_topk(const float *logits, int ld, int rows, const int32_t *idmap, int n, int k, int32_t *ids,
+                        float *vals, uint32_t *cand_k, uint32_t *cand_i, cudaStream_t st);
 
-cudaError_t launch_project(const ProjArgs &a, int grid, cudaStream_t st);
-cudaError_t launch_topk(const float *logits, int ld, const int32_t *count_ptr, int rows_host,
-                        const int32_t *idmap, int n, int k, int32_t *ids, float *vals, cudaStream_t st);
-
-size_t project_smem_bytes();
-cudaError_t prepare_project_kernels();
+// Dense head on tcgen05 (ns_dense.cu): logits[r, j] = hid[r, :] . W[j, :] for
+// r < n, j < rows, written to logits[r * ld + j]; W 16-byte aligned, H a
+// multiple of 64.  The top-k is a separate launch_topk.
+cudaError_t prepare_dense_kernel();
+cudaError_t launch_dense(const uint16_t *W, int rows, const uint16_t *hid, int n, int H, float *logits, int ld,
+                         uint32_t *err, cudaStream_t st);
 
 // Fused gather + projection + top-k on tcgen05 tensor cores (ns_umma.cu).
 struct UmmaLaunch {
