@@ -308,6 +308,23 @@ NS_API ns_status ns_sub_lm_head_indexed_topk(ns_handle *h, int32_t seq, const ui
 NS_API ns_status ns_set_copy_ctas(ns_handle *h, int32_t ctas);
 
 /*
+ * ns_step with the step's inputs and outputs in host memory: on `stream` it
+ * copies the tree ids (int32 [n_tree]), the verify row (fp32 [V], ignored
+ * when K_ver = 0) and the hidden rows (bf16 [n x H]) into the handle's
+ * device staging buffers, runs ns_step on them (logits in the handle's
+ * scratch), and copies the top-k ids and values (int32 / fp32 [n x k]) back
+ * to h_topk_ids / h_topk_vals.  It returns once everything is enqueued; the
+ * outputs are valid after the stream synchronises.  Host buffers should be
+ * pinned (page-locked) for the copies to run asynchronously; they must stay
+ * valid until then.  d_W_head is device memory as in ns_step.  With trace
+ * events set (ns_trace_events) the four events bracket the input copies,
+ * the step and the output copies.  Arguments as in ns_step.
+ */
+NS_API ns_status ns_step_host(ns_handle *h, int32_t seq, const int32_t *h_tree_ids, int32_t n_tree,
+                              const float *h_verify_row, const uint16_t *d_W_head, const uint16_t *h_hidden,
+                              int32_t n, int32_t k, int32_t *h_topk_ids, float *h_topk_vals, ns_stream stream);
+
+/*
  * Slot-stable packed buffer: the incremental reading of NanoSpec's
  * "Avoiding Sparse Computation via Asynchronous Gathering" (only the weights
  * of newly active tokens are gathered into the pre-allocated contiguous

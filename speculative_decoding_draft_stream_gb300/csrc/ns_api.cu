@@ -45,6 +45,12 @@ struct ns_handle {
   long long u_block_words = 0;  // one sequence's block: keys, ids, tickets
   cudaEvent_t trace[4] = {nullptr, nullptr, nullptr, nullptr};
   bool tracing = false;
+  // device staging of ns_step_host: tree ids, verify row, hidden rows, top-k
+  int32_t *st_tree = nullptr;
+  float *st_verify = nullptr;
+  uint16_t *st_hidden = nullptr;
+  int32_t *st_ids = nullptr;
+  float *st_vals = nullptr;
   long long seq_bytes = 0;  // distance between consecutive sequences' state
 };
 
@@ -117,6 +123,11 @@ void layout(ns_handle *h, Carver &cv) {
   }
   h->dense_ld = (c.V + 3) & ~3;
   h->dense_logits = cv.take<float>((size_t)ns::kProjBN * h->dense_ld);
+  h->st_tree = cv.take<int32_t>(c.max_tree > 0 ? c.max_tree : 1);
+  h->st_verify = cv.take<float>(c.K_ver > 0 ? c.V : 1);
+  h->st_hidden = cv.take<uint16_t>((size_t)NS_MAX_ROWS * c.H);
+  h->st_ids = cv.take<int32_t>((size_t)NS_MAX_ROWS * c.max_k);
+  h->st_vals = cv.take<float>((size_t)NS_MAX_ROWS * c.max_k);
   const size_t ncand = (size_t)NS_MAX_ROWS * ns::topk_slices(c.V) * NS_MAX_TOPK;
   h->dense_cand_k = cv.take<uint32_t>(ncand);
   h->dense_cand_i = cv.take<uint32_t>(ncand);
@@ -387,6 +398,11 @@ ns_status ns_sub_lm_head_indexed_topk(ns_handle *h, int32_t seq, const uint16_t 
                                             Rows::kIndexed));
 }
 
+static cudaError_t enqueue_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
+                                const float *d_verify_logits, int32_t verify_row, const uint16_t *d_W_head,
+                                const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits, int32_t ld_logits,
+                                int32_t *d_topk_ids, float *d_topk_vals, cudaStream_t cs, bool tr);
+
 ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
                   const float *d_verify_logits, int32_t n_verify, int32_t verify_row, const uint16_t *d_W_head,
                   const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits, int32_t ld_logits,
@@ -395,8 +411,17 @@ ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t 
   if (st != NS_OK) return st;
   st = check_gather_project_args(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals);
   if (st != NS_OK) return st;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const bool tr = h->tracing;
+  return cuda_status(enqueue_step(h, seq, d_tree_ids, n_tree, d_verify_logits, verify_row, d_W_head, d_hidden, n, k,
+                                  d_logits, ld_logits, d_topk_ids, d_topk_vals, static_cast<cudaStream_t>(stream),
+                                  h->tracing));
+}
+
+// The step's launches on cs (arguments checked by the caller); with `tr`
+// the four trace events bracket them.
+static cudaError_t enqueue_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
+                                const float *d_verify_logits, int32_t verify_row, const uint16_t *d_W_head,
+                                const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits, int32_t ld_logits,
+                                int32_t *d_topk_ids, float *d_topk_vals, cudaStream_t cs, bool tr) {
   cudaError_t e = tr ? trace_record(h->trace[0], cs) : cudaSuccess;
   const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
   if (h->step_clusters > 0) {  // one launch: state update, gather, projection, top-k
@@ -422,13 +447,43 @@ ns_status ns_step(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t 
     if (e == cudaSuccess) e = ns::launch_step(L, cs);
     if (e == cudaSuccess && tr) e = trace_record(h->trace[2], cs);
     if (e == cudaSuccess && tr) e = trace_record(h->trace[3], cs);
-    return cuda_status(e);
+    return e;
   }
   if (e == cudaSuccess) e = ns::launch_append(h->seqs[seq], h->dims, d_tree_ids, n_tree, zrow, true, h->err, cs);
   if (e == cudaSuccess && tr) e = trace_record(h->trace[1], cs);
   if (e == cudaSuccess)
     e = enqueue_gather_project(h, seq, d_W_head, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals, cs,
                                tr ? h->trace[2] : nullptr, !tr);
+  if (e == cudaSuccess && tr) e = trace_record(h->trace[3], cs);
+  return e;
+}
+
+ns_status ns_step_host(ns_handle *h, int32_t seq, const int32_t *h_tree_ids, int32_t n_tree,
+                       const float *h_verify_row, const uint16_t *d_W_head, const uint16_t *h_hidden, int32_t n,
+                       int32_t k, int32_t *h_topk_ids, float *h_topk_vals, ns_stream stream) {
+  ns_status st = check_append_args(h, seq, h->st_tree, n_tree, h->st_verify, 1, 0);
+  if (st != NS_OK) return st;
+  if ((n_tree > 0 && !h_tree_ids) || (h->cfg.K_ver > 0 && !h_verify_row) || !h_hidden || !h_topk_ids ||
+      !h_topk_vals)
+    return NS_ERR_ARG;
+  st = check_gather_project_args(h, seq, d_W_head, h->st_hidden, n, k, nullptr, 0, h->st_ids, h->st_vals);
+  if (st != NS_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const bool tr = h->tracing;
+  cudaError_t e = tr ? trace_record(h->trace[0], cs) : cudaSuccess;
+  if (e == cudaSuccess && n_tree > 0)
+    e = cudaMemcpyAsync(h->st_tree, h_tree_ids, (size_t)n_tree * 4, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess && h->cfg.K_ver > 0)
+    e = cudaMemcpyAsync(h->st_verify, h_verify_row, (size_t)h->cfg.V * 4, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(h->st_hidden, h_hidden, (size_t)n * h->cfg.H * 2, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess && tr) e = trace_record(h->trace[1], cs);
+  if (e == cudaSuccess)
+    e = enqueue_step(h, seq, h->st_tree, n_tree, h->st_verify, 0, d_W_head, h->st_hidden, n, k, nullptr, 0,
+                     h->st_ids, h->st_vals, cs, false);
+  if (e == cudaSuccess && tr) e = trace_record(h->trace[2], cs);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h_topk_ids, h->st_ids, (size_t)n * k * 4, cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h_topk_vals, h->st_vals, (size_t)n * k * 4, cudaMemcpyDeviceToHost, cs);
   if (e == cudaSuccess && tr) e = trace_record(h->trace[3], cs);
   return cuda_status(e);
 }

@@ -35,7 +35,7 @@ EXPORTED = (
     "ns_dense_lm_head_topk", "ns_get_active", "ns_get_state", "ns_get_error", "ns_state_update",
     "ns_gather_sub_lm_head_topk", "ns_trace_events", "ns_dense_lm_head_topk_noalloc", "ns_gather_new_head_rows",
     "ns_slot_lm_head_logits_topk", "ns_step_slots", "ns_get_slots", "ns_step_batch", "ns_sub_lm_head_indexed_topk",
-    "ns_step_launches", "ns_step_batch_union", "ns_get_union", "ns_set_copy_ctas",
+    "ns_step_launches", "ns_step_batch_union", "ns_get_union", "ns_set_copy_ctas", "ns_step_host",
 )
 NOALLOC_MAX_LOGITS = 1 << 20
 
@@ -70,6 +70,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "ns_device_bytes": (I64, [P]),
         "ns_step_launches": (I32, [P]),
         "ns_set_copy_ctas": (I32, [P, I32]),
+        "ns_step_host": (I32, [P, I32, P, I32, P, U16P, P, I32, I32, P, P, P]),
         "ns_stream_init": (I32, [P, I32, P, I32, P, P]),
         "ns_stream_append": (I32, [P, I32, P, I32, P, I32, I32, P]),
         "ns_build_active_vocab": (I32, [P, I32, P]),
@@ -244,6 +245,22 @@ class Handle:
                                  _ptr(logits, torch.float32, "logits"), ld, _ptr(ids, torch.int32, "ids"),
                                  _ptr(vals, torch.float32, "vals"), _stream(stream)), "ns_step")
         return ids, vals
+
+    def step_host(self, seq: int, tree_ids: Optional[torch.Tensor], verify_row: Optional[torch.Tensor],
+                  W_head: torch.Tensor, hidden: torch.Tensor, k: int, ids: torch.Tensor, vals: torch.Tensor,
+                  stream=None) -> None:
+        """ns_step_host: tree_ids int32 [n_tree], verify_row fp32 [V] and hidden bf16 [n, H] in (pinned) host
+        memory, ids int32 / vals fp32 [n, k] host outputs, valid once the stream synchronises."""
+        def host(t, what):
+            if t is None:
+                return None
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{what} must be a contiguous host tensor")
+            return t.data_ptr()
+        n_tree = 0 if tree_ids is None else tree_ids.numel()
+        _check(self._lib.ns_step_host(self._h, seq, host(tree_ids, "tree_ids"), n_tree, host(verify_row, "verify_row"),
+                                      _ptr(W_head, _BF16, "W_head"), host(hidden, "hidden"), hidden.shape[0], k,
+                                      host(ids, "ids"), host(vals, "vals"), _stream(stream)), "ns_step_host")
 
     def step_batch(self, tree_ids: Optional[torch.Tensor], verify_logits: Optional[torch.Tensor], verify_rows,
                    W_head: torch.Tensor, hidden: torch.Tensor, k: int, logits: Optional[torch.Tensor] = None,

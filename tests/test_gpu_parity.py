@@ -403,3 +403,35 @@ def test_trace_events_bracket_the_step(pkg):
             I = check_state(h, 0, o)
             check_projection(logits, ids, vals, hid, W, I, cfg.k)
         assert h._lib.ns_trace_events(h._h, None, 3) == -1  # wrong event count
+
+
+def test_step_host_equals_step(pkg):
+    """ns_step_host (inputs and outputs in pinned host memory, copies on the
+    stream) gives ns_step's window, I_t and top-k, bit for bit, on every step."""
+    cfg = MID
+    wl = Workload(cfg)
+    W_dev = dev_bf16(wl.w_head())
+    k = cfg.k
+    with _handle(pkg, cfg) as ha, _handle(pkg, cfg) as hb:
+        prompt, Z = wl.prompt(0), wl.prefill_logits(0)
+        for h in (ha, hb):
+            h.stream_init(0, dev_i32(prompt), dev_f32(Z))
+            h.build_active_vocab(0)
+        ids_h = torch.empty((cfg.n_tree, k), dtype=torch.int32).pin_memory()
+        vals_h = torch.empty((cfg.n_tree, k), dtype=torch.float32).pin_memory()
+        for t in range(cfg.steps):
+            tree, vb, vr, hid = wl.trees(0)[t], wl.verify_logits(0, t), wl.verify_row(0, t), wl.hiddens(0, t)
+            ids_b, vals_b = hb.step(0, dev_i32(tree), dev_f32(vb), vr, W_dev, dev_bf16(hid), k)
+            ha.step_host(0, torch.from_numpy(np.ascontiguousarray(tree)).pin_memory(),
+                         torch.from_numpy(np.ascontiguousarray(vb[vr])).pin_memory(), W_dev,
+                         torch.from_numpy(np.ascontiguousarray(hid).view(np.int16)).pin_memory(), k, ids_h, vals_h)
+            torch.cuda.synchronize()
+            assert torch.equal(ids_h, ids_b.cpu()), f"step {t}: top-k ids"
+            assert torch.equal(vals_h, vals_b.cpu()), f"step {t}: top-k values"
+            ia, ca, ba, _ = ha.get_active(0)
+            ib, cb, bb, _ = hb.get_active(0)
+            m = int(ca.item())
+            assert m == int(cb.item()) and torch.equal(ia[:m], ib[:m]) and torch.equal(ba, bb), f"step {t}: I_t"
+        assert ha.get_error() == 0 and hb.get_error() == 0
+        with pytest.raises(ValueError):  # device tensors are not host buffers
+            ha.step_host(0, dev_i32(wl.trees(0)[0]), None, W_dev, dev_bf16(wl.hiddens(0, 0)), k, ids_h, vals_h)

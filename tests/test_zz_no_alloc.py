@@ -4,12 +4,11 @@ ns_dense_lm_head_topk_noalloc exists for callers that cannot allocate device
 memory (and so cannot create a handle): it keeps its scratch in a fixed
 array inside the library.  These checks call it through the C ABI twice in a
 row (the second call finds the first call's leftovers in the scratch) and
-compare it with ns_dense_lm_head_topk on the same inputs, within the logits
-tolerance of the other tests, and with the CPU oracle's dense logits and
-top-k rule.  The two CUDA paths split the sum over H differently, so their
-logits agree to rounding and their top-k ids may swap between near-equal
-logits; the top-k rule allows exactly that.  This file sorts last so that a
-run stopping at the first failure has run everything else.
+compare it with ns_dense_lm_head_topk on the same inputs and with the CPU
+oracle's dense logits and top-k rule.  The two CUDA paths run the same
+kernels, so their logits and top-k must be equal bit for bit.  This file
+sorts last so that a run stopping at the first failure has run everything
+else.
 """
 
 import numpy as np
@@ -39,8 +38,8 @@ def ns():
     return nanospec
 
 
-# 1000 rows: fewer row tiles than CTAs, so K is split and the partial tiles
-# and arrival counters in the scratch are used; 17000 rows: one split per tile.
+# 1000 rows: a partial last row tile and a single, partial top-k slice;
+# 17000 rows: several slices, the last one partial.
 @pytest.mark.parametrize("rows", [1000, 17000])
 def test_noalloc_matches_handle_path_twice(ns, rows):
     wl = Workload(CFG)
@@ -63,7 +62,8 @@ def test_noalloc_matches_handle_path_twice(ns, rows):
             torch.cuda.synchronize()
             got = out_logits.cpu().numpy()
             ref = ref_logits.cpu().numpy()
-            # against the handle's dense head, within the logits tolerance
+            # against the handle's dense head: the same kernels, the same bits
+            assert np.array_equal(got, ref), "logits differ from the handle's dense head"
             tol_ref = check_logits(got, ref)
             # against the oracle: logits, and the top-k rule on its logits
             want = oracle.dense_logits(hid, W[:rows])
@@ -73,7 +73,7 @@ def test_noalloc_matches_handle_path_twice(ns, rows):
                     continue
                 check_topk(ids.cpu().numpy(), vals.cpu().numpy(), want, np.arange(rows), k, tol)
                 check_topk(ids.cpu().numpy(), vals.cpu().numpy(), ref, np.arange(rows), k, tol_ref)
-                assert torch.allclose(vals, ref_vals, rtol=0, atol=float(tol_ref.max()))
+                assert torch.equal(ids, ref_ids) and torch.equal(vals, ref_vals), "top-k differs from the handle's"
         assert h.get_error() == 0
 
 
