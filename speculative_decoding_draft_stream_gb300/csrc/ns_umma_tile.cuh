@@ -290,13 +290,18 @@ __device__ __forceinline__ void umma_tile(const UmmaSmem &S, uint32_t tmem, cons
   (void)s_ids;
 
   // ---- main loop -------------------------------------------------------------
-  if (warp == 0 && lane == 0) {  // hidden slices by TMA
+  // In place, row j of the tile is row row0 + j of the buffer tmP maps, so the
+  // rows of a stage are one tiled TMA load (the rows past |I_t| are loaded
+  // too and never ranked); otherwise the gather warps copy them by id.
+  const bool tma_rows = kInPlace && !a.rows_by_id;
+  if (warp == 0 && lane == 0) {  // hidden slices (and, in place, the row tiles) by TMA
     int issued = 0;
     for (int kt = 0; kt < nk; ++kt) {
       const int g = iter * nk + kt, s = g % kUStages;
       if (g >= kUStages && !mbar_wait(bar_empty + 8 * s, ((g / kUStages) - 1) & 1, a.err)) break;
       issued = kt + 1;
-      mbar_expect_tx(bar_full + 8 * s, kStageB);
+      mbar_expect_tx(bar_full + 8 * s, tma_rows ? kStage : kStageB);
+      if (tma_rows) tma_load_2d(base + s * kStage, &tmP, ((int)crank + kt * kUCluster) * kUK, row0, bar_full + 8 * s);
       if (kBatch)
         tma_load_3d(base + s * kStage + kStageA, &tmH, ((int)crank + kt * kUCluster) * kUK, 0, bseq,
                     bar_full + 8 * s);
@@ -319,14 +324,17 @@ __device__ __forceinline__ void umma_tile(const UmmaSmem &S, uint32_t tmem, cons
       if (g >= kUStages) mbar_wait(bar_empty + 8 * s, ((g / kUStages) - 1) & 1, a.err);
       const uint32_t A = base + s * kStage;
       const int col = ((int)crank + kt * kUCluster) * kUK + c * 8;
+      if (!tma_rows) {
 #pragma unroll
-      for (int rg = 0; rg < kUM / (4 * kGatherWarps); ++rg) {
-        const int row = (rg * kGatherWarps + wl) * 4 + (lane >> 3);
-        const uint16_t *src = a.W + (size_t)s_rows[row] * a.H + col;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(A + row * 128 + ((c ^ (row & 7)) << 4)),
-                     "l"(src)
-                     : "memory");
+        for (int rg = 0; rg < kUM / (4 * kGatherWarps); ++rg) {
+          const int row = (rg * kGatherWarps + wl) * 4 + (lane >> 3);
+          const uint16_t *src = a.W + (size_t)s_rows[row] * a.H + col;
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(A + row * 128 + ((c ^ (row & 7)) << 4)),
+                       "l"(src)
+                       : "memory");
+        }
       }
+      // (with no copy of this thread in flight the arrival is immediate)
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar_full + 8 * s) : "memory");
     }
     asm volatile("cp.async.wait_all;" ::: "memory");  // nothing of this thread is still landing
