@@ -360,15 +360,34 @@ NS_API ns_status ns_slot_lm_head_logits_topk(ns_handle *h, int32_t seq, const ui
                                              float *d_topk_vals, ns_stream stream);
 
 /*
- * One decode step on the slot buffer: ns_state_update, ns_gather_new_head_rows
- * and ns_slot_lm_head_logits_topk in order on `stream` (three kernels and the
- * row copy).  Arguments as ns_step; the logits are indexed by slot.
+ * One decode step on the slot buffer, with the results of
+ * ns_state_update, ns_gather_new_head_rows and ns_slot_lm_head_logits_topk
+ * made in order on `stream` (the slot table, the slot rows, the copied-row
+ * list and I_t included).  Arguments as ns_step; the logits are indexed by
+ * slot, and columns of free slots below the high-water mark hold NaN.
+ * When the slot table matches the window (the last call that changed this
+ * sequence's window was a slot update: ns_gather_new_head_rows or
+ * ns_step_slots) and the device holds the grid, it is ONE cooperative
+ * launch (ns_step_slots_fused returns 1): the tiles of the occupied slots
+ * are projected from the slot buffer while the window is updated, the ids
+ * that enter take their slots and are projected by the draft item and the
+ * verify products, and only their rows are copied.  Otherwise (after
+ * ns_stream_init, ns_stream_append, ns_state_update, ns_step, ns_step_host
+ * or a batched step) it is the three calls in order.
  */
 NS_API ns_status ns_step_slots(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, int32_t n_tree,
                                const float *d_verify_logits, int32_t n_verify, int32_t verify_row,
                                const uint16_t *d_W_head, const uint16_t *d_hidden, int32_t n, int32_t k,
                                float *d_logits, int32_t ld_logits, int32_t *d_topk_ids, float *d_topk_vals,
                                ns_stream stream);
+
+/*
+ * 1 when the next ns_step_slots on `seq` runs as one launch (the calls
+ * enqueued so far leave the slot table matching the window, and the device
+ * holds the grid), else 0 (also for a NULL handle or a bad seq).  Host
+ * bookkeeping only; no device work.
+ */
+NS_API int32_t ns_step_slots_fused(const ns_handle *h, int32_t seq);
 
 /*
  * Per-kernel event trace (MicroSpec §4 profiles per-step latency with CUDA

@@ -31,6 +31,12 @@ struct ns_handle {
   int step_clusters = 0;  // clusters of the one-launch step (0: two launches)
   int step_tpc = 0;       // tiles per cluster of the one-launch step
   int step_cl = 0;        // CTAs per cluster of the one-launch step
+  int slot_clusters = 0;  // the same for the one-launch slot-stable step (0: the multi-launch chain)
+  int slot_tpc = 0;
+  int slot_cl = 0;
+  // per sequence: the slot table matches the window (the calls enqueued so
+  // far end with a slot update; any later change of the window clears it)
+  std::vector<char> slots_synced;
   // union of the sequences' active vocabularies (batch > 1): its bitmap, ids
   // and count, the packed rows W_head[U, :], logits scratch and, per
   // sequence, candidate lists and tickets of the union projection
@@ -104,6 +110,9 @@ void layout(ns_handle *h, Carver &cv) {
     s.new_slot = cv.take<int32_t>(c.W_max);
     s.new_id = cv.take<int32_t>(c.W_max);
     s.slot_rows = cv.take<uint16_t>((size_t)c.W_max * c.H);
+    s.slot_of = cv.take<int32_t>(c.V);
+    s.slot_free = cv.take<uint32_t>(ns::slot_words(c.W_max));
+    s.slot_len = cv.take<long long>(1);
     s.gbar = cv.take<unsigned long long>(1);
     s.vcand_k = cv.take<uint32_t>((size_t)ns::kMaxStepCtas * (c.K_ver > 0 ? c.K_ver : 1));
     s.vcand_i = cv.take<uint32_t>((size_t)ns::kMaxStepCtas * (c.K_ver > 0 ? c.K_ver : 1));
@@ -206,20 +215,28 @@ ns_status ns_create(const ns_config *cfg, ns_handle **out) {
     return NS_ERR_CUDA;
   }
   h->inited.assign(c.batch, 0);
-  // The one-launch step needs every CTA of its grid resident at once (a
+  h->slots_synced.assign(c.batch, 0);
+  // The one-launch steps need every CTA of their grid resident at once (a
   // cooperative launch); check once that the device takes such a launch.
-  h->step_clusters = ns::step_plan(d, &h->step_tpc, &h->step_cl);
-  if (h->step_clusters > 0) {
-    ns::StepLaunch L{};
-    L.s = h->seqs[0];
-    L.d = d;
-    L.clusters = h->step_clusters;
-    L.tiles_per_cluster = h->step_tpc;
-    L.cluster_size = h->step_cl;
-    L.probe = true;
-    if (ns::launch_step(L, nullptr) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
-      cudaGetLastError();
-      h->step_clusters = 0;
+  for (int v = 0; v < 2; ++v) {
+    const bool slots = v == 1;
+    int &ncl = slots ? h->slot_clusters : h->step_clusters;
+    int &tpc = slots ? h->slot_tpc : h->step_tpc;
+    int &cl = slots ? h->slot_cl : h->step_cl;
+    ncl = ns::step_plan(d, slots, &tpc, &cl);
+    if (ncl > 0) {
+      ns::StepLaunch L{};
+      L.s = h->seqs[0];
+      L.d = d;
+      L.clusters = ncl;
+      L.tiles_per_cluster = tpc;
+      L.cluster_size = cl;
+      L.probe = true;
+      L.slots = slots;
+      if (ns::launch_step(L, nullptr) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        ncl = 0;
+      }
     }
   }
   *out = h;
@@ -238,6 +255,11 @@ int64_t ns_device_bytes(const ns_handle *h) { return h ? (int64_t)h->bytes : 0; 
 
 int32_t ns_step_launches(const ns_handle *h) { return h ? (h->step_clusters > 0 ? 1 : 2) : 0; }
 
+int32_t ns_step_slots_fused(const ns_handle *h, int32_t seq) {
+  if (!valid_seq(h, seq)) return 0;
+  return h->slot_clusters > 0 && h->slots_synced[seq] ? 1 : 0;
+}
+
 ns_status ns_stream_init(ns_handle *h, int32_t seq, const int32_t *d_prompt, int32_t L,
                          const float *d_prefill_logits, ns_stream stream) {
   if (!valid_seq(h, seq) || L < 0 || L > h->cfg.max_prompt || (L > 0 && !d_prompt)) return NS_ERR_ARG;
@@ -245,6 +267,7 @@ ns_status ns_stream_init(ns_handle *h, int32_t seq, const int32_t *d_prompt, int
   ns_status st = cuda_status(ns::launch_init(h->seqs[seq], h->dims, d_prompt, L, d_prefill_logits, h->err,
                                              static_cast<cudaStream_t>(stream)));
   if (st == NS_OK) h->inited[seq] = 1;
+  h->slots_synced[seq] = 0;  // the table is empty, the window is not
   return st;
 }
 
@@ -263,6 +286,7 @@ ns_status ns_stream_append(ns_handle *h, int32_t seq, const int32_t *d_tree_ids,
   ns_status st = check_append_args(h, seq, d_tree_ids, n_tree, d_verify_logits, n_verify, verify_row);
   if (st != NS_OK) return st;
   const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
+  h->slots_synced[seq] = 0;
   return cuda_status(ns::launch_append(h->seqs[seq], h->dims, d_tree_ids, n_tree, zrow, false, h->err,
                                        static_cast<cudaStream_t>(stream)));
 }
@@ -363,6 +387,7 @@ ns_status ns_state_update(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, 
   ns_status st = check_append_args(h, seq, d_tree_ids, n_tree, d_verify_logits, n_verify, verify_row);
   if (st != NS_OK) return st;
   const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
+  h->slots_synced[seq] = 0;
   return cuda_status(ns::launch_append(h->seqs[seq], h->dims, d_tree_ids, n_tree, zrow, true, h->err,
                                        static_cast<cudaStream_t>(stream)));
 }
@@ -422,6 +447,7 @@ static cudaError_t enqueue_step(ns_handle *h, int32_t seq, const int32_t *d_tree
                                 const float *d_verify_logits, int32_t verify_row, const uint16_t *d_W_head,
                                 const uint16_t *d_hidden, int32_t n, int32_t k, float *d_logits, int32_t ld_logits,
                                 int32_t *d_topk_ids, float *d_topk_vals, cudaStream_t cs, bool tr) {
+  h->slots_synced[seq] = 0;
   cudaError_t e = tr ? trace_record(h->trace[0], cs) : cudaSuccess;
   const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
   if (h->step_clusters > 0) {  // one launch: state update, gather, projection, top-k
@@ -501,6 +527,7 @@ ns_status ns_gather_new_head_rows(ns_handle *h, int32_t seq, const uint16_t *d_W
   if (!h->inited[seq]) return NS_ERR_STATE;
   cudaStream_t st = static_cast<cudaStream_t>(copy_stream);
   cudaError_t e = ns::launch_slot_update(h->seqs[seq], h->dims, d_W_head, h->sgrid, h->err, st);
+  h->slots_synced[seq] = e == cudaSuccess ? 1 : 0;
   if (e == cudaSuccess && done) e = cudaEventRecord(static_cast<cudaEvent_t>(done), st);
   return cuda_status(e);
 }
@@ -527,11 +554,38 @@ ns_status ns_step_slots(ns_handle *h, int32_t seq, const int32_t *d_tree_ids, in
   if (st != NS_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const float *zrow = h->cfg.K_ver > 0 ? d_verify_logits + (size_t)verify_row * h->cfg.V : nullptr;
-  cudaError_t e = ns::launch_append(h->seqs[seq], h->dims, d_tree_ids, n_tree, zrow, true, h->err, cs);
-  if (e == cudaSuccess) e = ns::launch_slot_update(h->seqs[seq], h->dims, d_W_head, h->sgrid, h->err, cs);
-  if (e == cudaSuccess)
-    e = enqueue_gather_project(h, seq, nullptr, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals, cs,
-                               nullptr, true, Rows::kSlots);
+  cudaError_t e = cudaSuccess;
+  if (h->slot_clusters > 0 && h->slots_synced[seq]) {
+    // one launch: the state and slot updates, the new rows' copy, the
+    // projection of the slot buffer and the top-k
+    ns::StepLaunch L{};
+    L.s = h->seqs[seq];
+    L.d = h->dims;
+    L.W = d_W_head;
+    L.hid = d_hidden;
+    L.n = n;
+    L.k = k;
+    L.logits = d_logits ? d_logits : h->seqs[seq].logits;
+    L.ld = d_logits ? ld_logits : h->dims.ld_scratch;
+    L.out_ids = d_topk_ids;
+    L.out_vals = d_topk_vals;
+    L.err = h->err;
+    L.tree = d_tree_ids;
+    L.n_tree = n_tree;
+    L.zrow = zrow;
+    L.clusters = h->slot_clusters;
+    L.tiles_per_cluster = h->slot_tpc;
+    L.cluster_size = h->slot_cl;
+    L.slots = true;
+    e = ns::launch_step(L, cs);
+  } else {
+    e = ns::launch_append(h->seqs[seq], h->dims, d_tree_ids, n_tree, zrow, true, h->err, cs);
+    if (e == cudaSuccess) e = ns::launch_slot_update(h->seqs[seq], h->dims, d_W_head, h->sgrid, h->err, cs);
+    if (e == cudaSuccess)
+      e = enqueue_gather_project(h, seq, nullptr, d_hidden, n, k, d_logits, ld_logits, d_topk_ids, d_topk_vals, cs,
+                                 nullptr, true, Rows::kSlots);
+  }
+  h->slots_synced[seq] = e == cudaSuccess ? 1 : 0;
   return cuda_status(e);
 }
 
@@ -552,6 +606,7 @@ ns_status ns_step_batch(ns_handle *h, int32_t n_seq, const int32_t *d_tree_ids, 
   if (st != NS_OK) return st;
   for (int b = 0; b < n_seq; ++b)
     if (!h->inited[b]) return NS_ERR_STATE;
+  for (int b = 0; b < n_seq; ++b) h->slots_synced[b] = 0;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   for (int c0 = 0; c0 < n_seq && e == cudaSuccess; c0 += ns::kMaxBatchLaunch) {
@@ -616,6 +671,7 @@ ns_status ns_step_batch_union(ns_handle *h, int32_t n_seq, const int32_t *d_tree
   if (st != NS_OK) return st;
   for (int b = 0; b < n_seq; ++b)
     if (!h->inited[b]) return NS_ERR_STATE;
+  for (int b = 0; b < n_seq; ++b) h->slots_synced[b] = 0;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   // 1. every sequence's state update and its own I_t

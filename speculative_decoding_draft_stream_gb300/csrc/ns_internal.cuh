@@ -42,11 +42,17 @@ struct SeqDev {
   int32_t *new_slot;    // [W_max] (slot, id) of each row the last update gathered, in assignment order
   int32_t *new_id;      // [W_max]
   uint16_t *slot_rows;  // [W_max x H] bf16 slot buffer
+  int32_t *slot_of;     // [V] slot of each id that holds one (entries of other ids are stale)
+  uint32_t *slot_free;  // [slot_words(W_max)] bit s of word s/32: slot s < W_max is free (other bits 0)
+  long long *slot_len;  // [1] |S| at the last slot update (-1 after a reset: the table is empty)
   // one-launch step (ns_step.cu)
   unsigned long long *gbar;  // [1] grid barrier counter (grows by the grid size per step)
   uint32_t *vcand_k;         // [kMaxStepCtas x K_ver] each CTA's verify Top-K: order keys
   uint32_t *vcand_i;         //   and ids
 };
+
+// Words of a sequence's free-slot bitmap (a multiple of 4, for 16-byte copies).
+__host__ __device__ inline int slot_words(int W_max) { return (((W_max + 31) / 32) + 3) & ~3; }
 
 struct Dims {
   int32_t V, H, W_max, K_pre, K_ver, nwords, nwords_pad, ld_scratch;
@@ -68,6 +74,7 @@ __host__ __device__ inline SeqDev seq_at(SeqDev s, long long off) {
   move_ptr(s.cand_i, off), move_ptr(s.slice_ticket, off), move_ptr(s.slot_id, off), move_ptr(s.held, off);
   move_ptr(s.slot_meta, off), move_ptr(s.new_slot, off), move_ptr(s.new_id, off), move_ptr(s.slot_rows, off);
   move_ptr(s.gbar, off), move_ptr(s.vcand_k, off), move_ptr(s.vcand_i, off), move_ptr(s.active_len, off);
+  move_ptr(s.slot_of, off), move_ptr(s.slot_free, off), move_ptr(s.slot_len, off);
   return s;
 }
 
@@ -517,13 +524,14 @@ struct StepLaunch {
   const float *zrow;         // the verify row (null when K_ver = 0)
   int32_t clusters, tiles_per_cluster, cluster_size;  // from step_plan
   bool probe;                // launch check: every CTA returns at once
+  bool slots;                // the slot-stable variant (the slot table must match the window)
 };
 // Sets the kernel's shared-memory limit and counts its resident clusters.
 cudaError_t prepare_step_kernel();
 // Clusters of a step launch for these dimensions (0: the configuration needs
 // the two-launch path); *tiles_per_cluster gets the tiles each cluster runs,
 // *cluster_size its CTAs.
-int step_plan(const Dims &d, int *tiles_per_cluster, int *cluster_size);
+int step_plan(const Dims &d, bool slots, int *tiles_per_cluster, int *cluster_size);
 cudaError_t launch_step(const StepLaunch &L, cudaStream_t st);
 
 }  // namespace ns

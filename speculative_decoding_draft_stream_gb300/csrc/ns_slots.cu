@@ -29,7 +29,9 @@ constexpr int kCopyUnits = 4;  // 16-byte loads a lane keeps in flight
 __device__ __forceinline__ bool has_bit(const uint32_t *w, int id) { return (w[id >> 5] >> (id & 31)) & 1u; }
 
 // One CTA.  Reads I_t, |I_t| and the window bitmap; updates slot_id, held,
-// slot_meta and the list of rows to gather (new_slot / new_id).
+// slot_meta and the list of rows to gather (new_slot / new_id), and the
+// state the one-launch slot step keeps besides: the slot of each placed id
+// (slot_of), the free-slot bitmap and the |S| the table now matches.
 __global__ void __launch_bounds__(kSlotThreads) slot_update_kernel(SeqDev s, Dims d, uint32_t *err) {
   extern __shared__ uint4 s_dyn4[];  // the window bitmap, then `held` (nwords_pad words each)
   __shared__ int sh[kSlotThreads / kWarp];
@@ -107,9 +109,21 @@ __global__ void __launch_bounds__(kSlotThreads) slot_update_kernel(SeqDev s, Dim
     if (fresh && rank < n_new) {
       const int sl = s.new_slot[rank];
       s.slot_id[sl] = id;
+      s.slot_of[id] = sl;
       s.new_id[rank] = id;
     }
     placed += total;
+  }
+  __syncthreads();  // the table is final (global, this block)
+
+  // the free-slot bitmap of the final table: warp w of a round covers 32
+  // consecutive slots, one word
+  const int nfw = slot_words(d.W_max);
+  for (int s0 = 0; s0 < 32 * nfw; s0 += blockDim.x) {
+    const int sl = s0 + tid;
+    const bool is_free = sl < d.W_max && s.slot_id[sl] < 0;
+    const unsigned word = __ballot_sync(0xffffffffu, is_free);
+    if ((tid & (kWarp - 1)) == 0 && sl < 32 * nfw) s.slot_free[sl >> 5] = word;
   }
 
   // 4. held := the window bitmap; the high-water mark and the row count
@@ -120,6 +134,7 @@ __global__ void __launch_bounds__(kSlotThreads) slot_update_kernel(SeqDev s, Dim
     if (n_new > 0 && s.new_slot[n_new - 1] + 1 > top) top = s.new_slot[n_new - 1] + 1;
     s.slot_meta[0] = top;
     s.slot_meta[1] = n_new;
+    *s.slot_len = s.length[0];
   }
 }
 

@@ -151,8 +151,9 @@ __host__ __device__ inline int state_smem_words(int nwords_pad) { return 3 * nwo
 // ---------------------------------------------------------------------------
 // Entries the reset touches: the counts, the bitmaps and the slot table.
 __host__ __device__ inline int reset_extent(const Dims &d) {
-  const int n = d.V > d.nwords_pad ? d.V : d.nwords_pad;
-  return n > d.W_max ? n : d.W_max;
+  int n = d.V > d.nwords_pad ? d.V : d.nwords_pad;
+  n = n > d.W_max ? n : d.W_max;
+  return n > slot_words(d.W_max) ? n : slot_words(d.W_max);
 }
 
 // An empty stream: no entries, an empty window, and an empty slot table.
@@ -168,6 +169,10 @@ __global__ void init_reset_kernel(SeqDev s, Dims d) {
       s.held[i] = 0u;
     }
     if (i < d.W_max) s.slot_id[i] = -1;
+    if (i < slot_words(d.W_max)) {  // every slot free
+      const int b0 = 32 * i;
+      s.slot_free[i] = b0 >= d.W_max ? 0u : (d.W_max - b0 >= 32 ? 0xffffffffu : (1u << (d.W_max - b0)) - 1u);
+    }
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     s.length[0] = 0;
@@ -176,6 +181,7 @@ __global__ void init_reset_kernel(SeqDev s, Dims d) {
     *s.active_len = 0;  // the empty I_t matches the empty stream
     s.slot_meta[0] = 0;
     s.slot_meta[1] = 0;
+    *s.slot_len = -1;  // the empty table matches no window
     *s.gbar = 0ull;
   }
 }

@@ -45,6 +45,22 @@
 // new state all after it.  Every wait is bounded (about a second); a wait
 // that runs out sets NS_FLAG_TIMEOUT and the kernel still follows the same
 // barrier sequence.
+//
+// The slot-stable variant (kSlots) is the same step on the slot buffer of
+// NanoSpec's incremental gather (only the rows of newly active ids are
+// copied; an id keeps its row slot while it stays active).  It needs the
+// slot table to match the window at launch (the host takes the multi-launch
+// path otherwise).  Then a column's slot is known before the state update:
+//   * the old items are the tiles of slots [0, high-water mark), their rows
+//     read from the slot buffer itself; a slot whose id stays is written in
+//     place, a slot left free gets NaN (never ranked);
+//   * the state group frees the slots of the ids that leave and gives the
+//     entering ids the lowest free slots in ascending id order, so the draft
+//     item and the verify products write them at their new slots;
+//   * the row top-k maps a column to its id through the slot table, and the
+//     rows of the entering ids are copied into their slots once every CTA is
+//     past the second grid barrier (no tile reads a slot row any more).
+// No compaction is on the logits' path and there is no packed copy.
 #include <cuda.h>
 
 #include "ns_umma_tile.cuh"
@@ -99,6 +115,16 @@ struct StepArgs {
   const float *zrow;          // the verify row (null when K_ver = 0)
   int32_t K, nwords_pad, ring_words, items_per_cluster, t_max, vec;
   int32_t probe;              // launch check only: every CTA returns at once
+  // slot-stable variant only
+  int32_t *slot_id;           // [W_max] id a slot holds, -1 = free
+  int32_t *slot_of;           // [V] slot of each id that holds one
+  uint32_t *slot_free;        // [fs_words] bit s of word s/32: slot s < W_max is free
+  uint32_t *held;             // [nwords_pad] ids holding a slot (the window bitmap at the last slot update)
+  int32_t *slot_meta;         // [2] high-water mark, rows the last update copied
+  int32_t *new_slot, *new_id;  // [W_max] (slot, id) of those rows, in assignment order
+  uint16_t *slot_rows;        // [W_max x H]
+  long long *slot_len;        // [1] |S| at the last slot update
+  int32_t fs_words;           // words of slot_free (a multiple of 4)
 };
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
@@ -292,11 +318,16 @@ __device__ __forceinline__ int sg_exclusive_scan(int v, int *sh, int *total) {
 // Word offsets of the state group's arrays (the bulk-copy destinations need
 // 16-byte alignment).
 struct StepSmem {
-  int bits, ring, len, goff, vk, vi, hash, wl, small, share, total;
+  int bits, ring, len, goff, vk, vi, hash, wl, small, share, slot, total;
 };
+// The slot-stable variant's arrays (at L.slot): the free-slot words, their
+// exclusive prefix counts, two hash arrays (an evictable id's old slot, an
+// entering id's new slot) and five lists of the entering ids.
+constexpr int kSlotHashArrays = 2;
+constexpr int kSlotLists = 5;
 __host__ __device__ inline int round4(int x) { return (x + 3) & ~3; }
 __host__ __device__ inline int share_of(int W, int P) { return (W + P - 1) / P; }
-__host__ __device__ inline StepSmem step_smem(int nwords_pad, int ring_words, int W, int P, int K) {
+__host__ __device__ inline StepSmem step_smem(int nwords_pad, int ring_words, int W, int P, int K, bool slots) {
   StepSmem L;
   L.bits = 0;
   L.ring = L.bits + nwords_pad;                 // nwords_pad and ring_words are multiples of 4
@@ -308,14 +339,15 @@ __host__ __device__ inline StepSmem step_smem(int nwords_pad, int ring_words, in
   L.wl = L.hash + kHashArrays * kStepHash;
   L.small = L.wl + 2 * (kSgWarps + 1) * NS_MAX_SELECT_K + 2 * NS_MAX_SELECT_K;
   L.share = L.small + round4(NS_MAX_ROWS + 3 * kMaxAppendStep + 8 + kSgWarps + 3 * kVerPairs);
-  L.total = L.share + round4(share_of(W, P));
+  L.slot = L.share + round4(share_of(W, P));
+  L.total = L.slot + (slots ? 2 * slot_words(W) + kSlotHashArrays * kStepHash + kSlotLists * kMaxAppendStep : 0);
   return L;
 }
 __host__ __device__ inline int step_smem_bytes(const StepSmem &L) {
   return 1024 + kSRing + kMaxItemsPerCluster * kFBytes + kStepMiscBytes + 4 * L.total;
 }
 
-template <int kCL>
+template <int kCL, bool kSlots>
 __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
     step_kernel(const __grid_constant__ CUtensorMap tmH, StepArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -344,11 +376,12 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
   const uint32_t bar_acc = bar_empty + 8 * kSStages, bar_pready = bar_acc + 8, bar_pdone = bar_pready + 8;
   const uint32_t bar_old = bar_pdone + 8, bar_cver = bar_old + 8, bar_state = bar_cver + 8;
   const uint32_t bar_ring = bar_state + 8, bar_copy = bar_ring + 8, sbar = bar_copy + 8;
+  const uint32_t bar_tbl = sbar + 8, bar_k2 = bar_tbl + 8;  // slot-stable variant: table copy landed; past barrier 2
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc + 256);
-  int *s_flag = reinterpret_cast<int *>(misc + 272);   // [1] state failed, [2], [3] barrier words
+  int *s_flag = reinterpret_cast<int *>(misc + 272);   // [1] state failed, [2], [3] barrier words, [5] past barrier 2
   int *s_tiles = reinterpret_cast<int *>(misc + 512);  // [items][kUM] ids of the items' rows (-1: none)
   int32_t *wbase = reinterpret_cast<int32_t *>(misc + kStepMiscBytes);
-  const StepSmem L = step_smem(a.nwords_pad, a.ring_words, W, P, K);
+  const StepSmem L = step_smem(a.nwords_pad, a.ring_words, W, P, K, kSlots);
   uint32_t *s_bits = reinterpret_cast<uint32_t *>(wbase + L.bits);
   int32_t *s_ring = wbase + L.ring;
   long long *s_len = reinterpret_cast<long long *>(wbase + L.len);
@@ -364,6 +397,17 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
   int32_t *s_share = wbase + L.share;
   uint32_t *s_vk = reinterpret_cast<uint32_t *>(wbase + L.vk);
   uint32_t *s_vi = reinterpret_cast<uint32_t *>(wbase + L.vi);
+  // slot-stable variant: free slots (updated in place by the state group),
+  // their prefix counts, the hash arrays of old and new slots, the entering
+  // ids (as found, then ranked) and their new slots; the table of slot ids
+  // for the row top-k lives in the stage ring past the top-k lists
+  const int fsw = kSlots ? a.fs_words : 0;
+  uint32_t *s_fs = reinterpret_cast<uint32_t *>(wbase + L.slot);
+  int *s_fsp = reinterpret_cast<int *>(s_fs + fsw);
+  int *h_sold = s_fsp + fsw, *h_nslot = h_sold + kStepHash;
+  int *e_id = h_nslot + kStepHash, *e_h = e_id + kMaxAppendStep;
+  int *p_id = e_h + kMaxAppendStep, *p_slot = p_id + kMaxAppendStep, *p_h = p_slot + kMaxAppendStep;
+  int32_t *s_tbl = reinterpret_cast<int32_t *>(gbase + kCopyOff);
 
   const int nitems = a.items_per_cluster;
   const int t_max = a.t_max;
@@ -385,16 +429,22 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
     mbar_init(bar_state, 1);
     mbar_init(bar_ring, 1);
     mbar_init(bar_copy, 1);
+    if (kSlots) {
+      mbar_init(bar_tbl, 1);
+      mbar_init(bar_k2, 1);
+    }
     s_flag[1] = 0;
+    s_flag[4] = 0;
     mbar_fence_init();
   }
   if (tid == kKThreads) {  // the state group's copies leave first
     mbar_init(sbar, 1);
     mbar_fence_init();
-    mbar_expect_tx(sbar, (uint32_t)(a.nwords_pad + a.ring_words) * 4u + 16u);
+    mbar_expect_tx(sbar, (uint32_t)(a.nwords_pad + a.ring_words + fsw) * 4u + 16u);
     bulk_load(smem_u32(s_bits), a.bitmap, (uint32_t)a.nwords_pad * 4u, sbar);
     bulk_load(smem_u32(s_ring), a.ring, (uint32_t)a.ring_words * 4u, sbar);
     bulk_load(smem_u32(s_len), a.length, 16u, sbar);
+    if (kSlots) bulk_load(smem_u32(s_fs), a.slot_free, (uint32_t)fsw * 4u, sbar);
   }
   if (tid == 32) tma_prefetch(&tmH);
   // tile group: the ids of its items' rows (old items: I_{t-1}; the draft
@@ -403,7 +453,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
   int m_old = 0;
   long long built_len = 0, cur_len = 0;
   if (tgrp || vgrp) {  // compared after the setup barrier (the loads are in flight meanwhile)
-    m_old = *a.count;
+    m_old = kSlots ? a.slot_meta[0] : *a.count;  // slot-stable: the old items cover [0, high-water mark)
     built_len = *a.active_len;
     cur_len = a.length[0];
   }
@@ -414,7 +464,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
       const int it = cid + j * ncid;
       if (ttid < kUM && j < nitems) {
         if (it < t_max) {
-          if (it * kUM + ttid < W) t_id[j] = a.active[it * kUM + ttid];
+          if (it * kUM + ttid < W) t_id[j] = kSlots ? a.slot_id[it * kUM + ttid] : a.active[it * kUM + ttid];
         } else if (it == t_max && ttid < n_tree) {
           t_id[j] = a.tree[ttid];
         }
@@ -464,7 +514,9 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
   // every CTA of the cluster has initialized its barriers before the first
   // remote arrival (the tile group waits on this before its first one)
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  const bool stale = built_len != cur_len;  // I_{t-1} was not built from the current window (then the tiles wait for I_t)
+  // I_{t-1} was not built from the current window (then the tiles wait for
+  // I_t); the slot-stable variant's columns do not depend on I_{t-1}
+  const bool stale = !kSlots && built_len != cur_len;
 
   if (tgrp) {
     // ======================== tile group ======================================
@@ -518,6 +570,9 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
         }
       } else if (warp >= 4) {  // W_head rows by cp.async (rows without an id stay unread)
         const int p = tid - 128, wl = p >> 5, c = lane & 7;
+        // the slot-stable variant's old items read the slot buffer's own rows
+        const bool from_slots = kSlots && it < t_max;
+        const uint16_t *src0 = from_slots ? a.slot_rows + (size_t)it * kUM * H : u.W;
         for (int kt = 0; kt < nk; ++kt) {
           const int g = iter * nk + kt, s = g % kSStages;
           if (g >= kSStages) mbar_wait(bar_empty + 8 * s, ((g / kSStages) - 1) & 1, u.err);
@@ -529,7 +584,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
             const int id = rows[row];
             if (id >= 0)
               asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(A + row * 128 + ((c ^ (row & 7)) << 4)),
-                           "l"(u.W + (size_t)id * H + col)
+                           "l"(src0 + (size_t)(from_slots ? row : id) * H + col)
                            : "memory");
           }
           asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar_full + 8 * s) : "memory");
@@ -610,11 +665,59 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
     }
     if (!cluster_ready) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     if (ttid == 0) mbar_arrive(bar_ring);  // the ring is free past the top-k lists
+    if (kSlots && ttid == 0) {  // the old slot table, for the row top-k (its changed entries are patched below)
+      const int nt = round4(m_old < 0 ? 0 : (m_old > W ? W : m_old));
+      if (nt > 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect_tx(bar_tbl, (uint32_t)nt * 4u);
+        bulk_load(smem_u32(s_tbl), a.slot_id, (uint32_t)nt * 4u, bar_tbl);
+      } else {
+        mbar_arrive(bar_tbl);
+      }
+    }
 
     // ---- the columns at their positions in I_t ------------------------------
     const bool okst = mbar_wait(bar_state, 0, u.err);
     const int m_act = s_misc[3];
-    if (ttid < 2 * kUM && okst) {
+    if (kSlots && ttid < 2 * kUM && okst && m_act >= 0) {
+      // slot-stable: a slot whose id stays is written in place, a slot left
+      // free below the new high-water mark gets NaN, a slot an entering id
+      // took is left to the draft item or the verify products
+      const int col = ttid & (kUM - 1), rg = ttid / kUM;
+      for (int j = 0; j < nitems; ++j) {
+        const int it = cid + j * ncid;
+        const bool active = it < t_max ? it < t_old : (it == t_max && n_tree > 0);
+        if (!active) continue;
+        const int id = s_tiles[j * kUM + col];
+        int pos = -1;
+        bool hole = false;
+        if (it < t_max) {
+          const int sl = it * kUM + col;
+          if (id >= 0 && ((s_bits[id >> 5] >> (id & 31)) & 1u)) {
+            pos = sl;
+          } else if (sl < m_act && ((s_fs[sl >> 5] >> (sl & 31)) & 1u)) {
+            pos = sl;
+            hole = true;
+          }
+        } else if (id >= 0) {
+          const int h = hash_find(h_key, id);
+          if (h >= 0 && h_ent[h] != 0 && h_wrow[h] == col) pos = h_nslot[h];
+        }
+        if (pos >= 0 && pos < W) {
+          const float *F = Fbuf + j * kFRows * kUM;
+          for (int rr = rg; rr < nr; rr += 2)
+            if (r0 + rr < u.n)
+              u.logits[(size_t)(r0 + rr) * u.ld + pos] = hole ? __int_as_float(0x7fffffff) : F[rr * kUM + col];
+        }
+      }
+    }
+    if (kSlots) {  // the new slots of the entering ids into the table copy
+      if (ttid == 0 && !mbar_wait(bar_tbl, 0, u.err)) s_flag[4] = 1;
+      named_sync(kBarT, kTGroup);
+      const int n_new = okst && m_act >= 0 ? s_misc[4] : 0;
+      if (ttid < n_new && ttid < kMaxAppendStep && (unsigned)p_slot[ttid] < (unsigned)W) s_tbl[p_slot[ttid]] = p_id[ttid];
+    }
+    if (!kSlots && ttid < 2 * kUM && okst) {
       const int col = ttid & (kUM - 1), rg = ttid / kUM;  // one column per thread, two row groups
       for (int j = 0; j < nitems; ++j) {
         const int it = cid + j * ncid;
@@ -691,12 +794,18 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
       const int v = q / n, r = q - v * n, id = s_app[n_draft + v];
       const int h = hash_find(h_key, id);
       if (h >= 0 && h_ent[h] != 0 && h_wrow[h] == kVerRow0 + v) {
-        const uint32_t w = s_bits[id >> 5], bit = 1u << (id & 31);
-        const int g4 = id >> 7;
-        int pos = s_goff[g4];
-        for (int qq = 4 * g4; qq < (id >> 5); ++qq) pos += __popc(s_bits[qq]);
-        pos += __popc(w & (bit - 1u));
-        if (pos < m_act) u.logits[(size_t)r * u.ld + pos] = s_vdot[i];
+        int pos;
+        if (kSlots) {
+          pos = h_nslot[h];  // the slot it took
+          if (pos >= W) pos = -1;
+        } else {
+          const uint32_t w = s_bits[id >> 5], bit = 1u << (id & 31);
+          const int g4 = id >> 7;
+          pos = s_goff[g4];
+          for (int qq = 4 * g4; qq < (id >> 5); ++qq) pos += __popc(s_bits[qq]);
+          pos += __popc(w & (bit - 1u));
+        }
+        if (pos >= 0 && pos < m_act) u.logits[(size_t)r * u.ld + pos] = s_vdot[i];
       }
     }
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -706,8 +815,12 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
     // ---- every CTA's columns are out: rank whole rows ------------------------
     // (the bitmap and group counts of I_t in this CTA's shared memory map a
     // column back to its id)
-    const bool ok = grid_barrier(a.gbar, (unsigned long long)P, u.err, &s_flag[2], kBarK, kKThreads, tid == 0) &&
-                    s_misc[3] >= 0;
+    bool ok = grid_barrier(a.gbar, (unsigned long long)P, u.err, &s_flag[2], kBarK, kKThreads, tid == 0) &&
+              s_misc[3] >= 0;
+    if (kSlots) {
+      if (tid == 0) mbar_arrive(bar_k2);  // the state group may now write slot rows and the slot table
+      ok = ok && s_flag[4] == 0;          // the table copy landed
+    }
     const int m_act = s_misc[3];
     if (ok) {
       uint32_t *rk = reinterpret_cast<uint32_t *>(gbase);  // [(warps + 1) x k] lists, then the result
@@ -734,8 +847,17 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
 #pragma unroll
             for (int q = 0; q < 8; ++q) hk[q] = j0 + q < m_act ? order_key(__ldcg(row + j0 + q)) : 0u;
           }
+          if (kSlots) {  // slot-stable: rank by (value, id), the id from the slot table
 #pragma unroll
-          for (int q = 0; q < 8; ++q) hi[q] = hk[q] != 0u ? (uint32_t)(j0 + q) : (uint32_t)kEmptyId;
+            for (int q = 0; q < 8; ++q) {
+              const int idq = hk[q] != 0u ? s_tbl[j0 + q] : -1;
+              hi[q] = idq >= 0 ? (uint32_t)idq : (uint32_t)kEmptyId;
+              if (idq < 0) hk[q] = 0u;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) hi[q] = hk[q] != 0u ? (uint32_t)(j0 + q) : (uint32_t)kEmptyId;
+          }
           uint32_t wk, wi;
           warp_topk8_lanes(hk, hi, k, &wk, &wi);
           if (lane < k) {
@@ -756,7 +878,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
         if (tid < k) {  // column -> id through I_t
           const uint32_t key = rk[kKWarps * k + tid];
           const int jc = (int)ri[kKWarps * k + tid];
-          u.out_ids[r * k + tid] = key != 0u ? nth_id(s_bits, s_goff, a.nwords_pad / 4, jc) : -1;
+          u.out_ids[r * k + tid] = key == 0u ? -1 : (kSlots ? jc : nth_id(s_bits, s_goff, a.nwords_pad / 4, jc));
           u.out_vals[r * k + tid] = key != 0u ? key_value(key) : -__int_as_float(0x7f800000);
         }
         named_sync(kBarK, kKThreads);
@@ -773,6 +895,14 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
       h_wrow[q] = 0x7fffffff;
       h_ent[q] = 0;
       h_chg[q] = -1;
+      if (kSlots) {
+        h_sold[q] = -1;
+        h_nslot[q] = -1;
+      }
+    }
+    if (kSlots && stid == 0) {
+      s_misc[5] = 0;  // entering ids found
+      s_misc[6] = 0;  // new high-water mark
     }
     if (stid < n_tree) s_tree[stid] = tree_id;
     // the old window: |S|, its ring slot, the entries that may leave and
@@ -782,11 +912,14 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
     const bool have = s_flag[1] == 0;
     const long long len0 = s_len[0];
     const int head = (int)s_len[1];
+    // the slot table must match the window the step starts from (the host
+    // takes the multi-launch path otherwise)
+    if (kSlots && writer && stid == 0 && have && __ldcg(a.slot_len) != len0) set_flag(u.err, NS_FLAG_INTERNAL | (7u << 8));
     const long long old_start = len0 > W ? len0 - W : 0;
     const int n_old = (int)(len0 - old_start);
     int max_ev = n_tree + K;
     if (max_ev > n_old) max_ev = n_old;
-    int ev_id = -1;
+    int ev_id = -1, ev_slot = -1;
     uint32_t ev_cnt = 0u;
     if (stid < max_ev) {  // position old_start + stid
       const int slot = len0 > W ? (head + stid >= W ? head + stid - W : head + stid) : stid;
@@ -795,7 +928,10 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
         if (writer) set_flag(u.err, NS_FLAG_INTERNAL | (2u << 8));
         ev_id = -1;
       }
-      if (ev_id >= 0) ev_cnt = __ldcg(a.counts + ev_id);  // read before the grid barrier, used after it
+      if (ev_id >= 0) {  // read before the grid barrier, used after it
+        ev_cnt = __ldcg(a.counts + ev_id);
+        if (kSlots) ev_slot = __ldcg(a.slot_of + ev_id);  // an id in the window holds a slot
+      }
       s_evid[stid] = ev_id;
     }
 
@@ -866,7 +1002,10 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
     }
     if (ev_id >= 0) {  // the evictable ids and their window counts
       const int h = hash_insert(h_key, ev_id);
-      if (h >= 0) h_cnt[h] = (int)ev_cnt;  // every occurrence of an id read the same count
+      if (h >= 0) {
+        h_cnt[h] = (int)ev_cnt;  // every occurrence of an id read the same count
+        if (kSlots) h_sold[h] = ev_slot;
+      }
     }
 
     // ---- grid barrier: every CTA's Top-K is out, every old-state read done --
@@ -876,6 +1015,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
 
     // ---- C_ver, the window update, I_t --------------------------------------
     int m_act = 0;
+    long long len_new = 0;  // |S| after the append
     if (ok) {
       for (int q = stid; q < P * K; q += kSgThreads) {
         s_vk[q] = __ldcg(a.vk + q);
@@ -950,6 +1090,11 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
               atomicOr(&s_bits[id >> 5], bit);
               h_ent[q] = 1;
               h_chg[q] = id >> 5;
+              if (kSlots) {
+                const int e = atomicAdd(&s_misc[5], 1);  // fewer than kMaxAppendStep: one per appended id
+                e_id[e] = id;
+                e_h[e] = q;
+              }
             }
           } else if (ev > 0) {
             const int now = h_cnt[q] - ev;
@@ -957,6 +1102,11 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
             if (now <= 0) {
               atomicAnd(&s_bits[id >> 5], ~bit);
               h_chg[q] = id >> 5;
+              if (kSlots) {  // its slot is free again
+                const int sl = h_sold[q];
+                if ((unsigned)sl < (unsigned)W) atomicOr(&s_fs[sl >> 5], 1u << (sl & 31));
+                else if (writer) set_flag(u.err, NS_FLAG_INTERNAL | (8u << 8));
+              }
             }
           }
           if (writer && ap != ev) atomicAdd(&a.counts[id], (unsigned)(ap - ev));
@@ -974,6 +1124,66 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
       if (writer) {
         for (int q = stid; q < kStepHash; q += kSgThreads)
           if (h_chg[q] >= 0) a.bitmap[h_chg[q]] = s_bits[h_chg[q]];
+      }
+      len_new = len1;
+
+      if (kSlots) {
+        // ---- the slot update: the entering ids, ascending, take the lowest
+        // free slots (the slots of the ids that left are free again)
+        const int n_new = s_misc[5];
+        if (stid < n_new) {
+          const int id = e_id[stid];
+          int rk = 0;
+          for (int q = 0; q < n_new; ++q) rk += e_id[q] < id ? 1 : 0;
+          p_id[rk] = id;
+          p_h[rk] = e_h[stid];
+        }
+        const int G2 = (fsw + kSgThreads - 1) / kSgThreads;
+        int nfree_mine = 0;
+        for (int w = stid * G2; w < stid * G2 + G2 && w < fsw; ++w) nfree_mine += __popc(s_fs[w]);
+        int nfree;
+        int fo = sg_exclusive_scan(nfree_mine, sh_scan, &nfree);
+        for (int w = stid * G2; w < stid * G2 + G2 && w < fsw; ++w) {
+          s_fsp[w] = fo;
+          fo += __popc(s_fs[w]);
+        }
+        named_sync(kBarS, kSgThreads);
+        if (stid < n_new) {
+          int sl = -1;
+          if (stid < nfree) {  // the last word with fewer free slots before it than this rank
+            int lo_w = 0, hi_w = fsw - 1;
+            while (lo_w < hi_w) {
+              const int mid = (lo_w + hi_w + 1) >> 1;
+              if (s_fsp[mid] <= stid) lo_w = mid;
+              else hi_w = mid - 1;
+            }
+            sl = 32 * lo_w + select_bit(s_fs[lo_w], stid - s_fsp[lo_w]);
+          }
+          if ((unsigned)sl >= (unsigned)W) {  // more active ids than slots: cannot happen while |I_t| <= W_max
+            if (writer) set_flag(u.err, NS_FLAG_OVERFLOW);
+            sl = -1;
+          }
+          p_slot[stid] = sl;
+          h_nslot[p_h[stid]] = sl;
+        }
+        named_sync(kBarS, kSgThreads);
+        if (stid < n_new && p_slot[stid] >= 0) atomicAnd(&s_fs[p_slot[stid] >> 5], ~(1u << (p_slot[stid] & 31)));
+        named_sync(kBarS, kSgThreads);
+        int top = 0;  // one past the highest occupied slot
+        for (int w = stid; w < fsw; w += kSgThreads) {
+          const int b0 = 32 * w;
+          uint32_t occ = b0 < W ? ~s_fs[w] : 0u;
+          if (b0 < W && W - b0 < 32) occ &= (1u << (W - b0)) - 1u;
+          if (occ != 0u) top = b0 + 32 - __clz(occ);
+        }
+        if (top > 0) atomicMax(&s_misc[6], top);
+        named_sync(kBarS, kSgThreads);
+        if (stid == 0) {
+          s_misc[3] = s_misc[6];  // the columns the tile and verify groups write and the top-k ranks
+          s_misc[4] = n_new;
+        }
+        named_sync(kBarS, kSgThreads);
+        if (stid == 0) mbar_arrive(bar_state);  // the tile and verify groups may place their columns
       }
 
       // compaction: per 4-word group, the number of ids before it
@@ -993,13 +1203,13 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
         off += __popc(w4.x) + __popc(w4.y) + __popc(w4.z) + __popc(w4.w);
       }
       m_act = total < W ? total : W;
-      if (stid == 0) s_misc[3] = m_act;
+      if (!kSlots && stid == 0) s_misc[3] = m_act;
       if (writer && stid == 0) {
         if (total > W) set_flag(u.err, NS_FLAG_OVERFLOW);
         *a.count = m_act;
       }
       named_sync(kBarS, kSgThreads);
-      if (stid == 0) mbar_arrive(bar_state);  // the tile and verify groups may place their columns
+      if (!kSlots && stid == 0) mbar_arrive(bar_state);  // the tile and verify groups may place their columns
       // this CTA's share of I_t: positions [p0, p0 + share)
       const int share = share_of(W, P), p0 = cta * share;
       for (int i = stid; i < share; i += kSgThreads) {
@@ -1013,6 +1223,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
       }
     } else if (stid == 0) {
       s_misc[3] = -1;  // no columns, no ranking
+      s_misc[4] = 0;   // no new slots
       mbar_arrive(bar_cver);
       mbar_arrive(bar_state);
     }
@@ -1020,7 +1231,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
     // ---- the packed buffer: the rows of this CTA's share by bulk copies
     // through the stage ring (once the tile group is done with it), beside
     // the top-k
-    if (ok && stid == 0) {
+    if (!kSlots && ok && stid == 0) {
       const int share = share_of(W, P), p0 = cta * share;
       int nsh = m_act - p0;
       if (nsh > share) nsh = share;
@@ -1046,6 +1257,51 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
         bulk_wait_all();
       }
     }
+    if (kSlots && ok) {
+      // ---- slot-stable: once every CTA is past the second grid barrier (no
+      // tile reads a slot row or the old table any more), the entering ids'
+      // rows into their slots, and (the last CTA) the new slot state
+      if (stid == 0) s_flag[5] = mbar_wait(bar_k2, 0, u.err) ? 1 : 0;
+      named_sync(kBarS, kSgThreads);
+      if (s_flag[5]) {
+        const int n_new = s_misc[4];
+        const int upr = H >> 3;  // 16-byte units per row
+        for (int r = cta; r < n_new; r += P) {
+          const int id = p_id[r], sl = p_slot[r];
+          if ((unsigned)id < (unsigned)V && (unsigned)sl < (unsigned)W) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(u.W + (size_t)id * H);
+            uint4 *dst = reinterpret_cast<uint4 *>(a.slot_rows + (size_t)sl * H);
+#pragma unroll 4
+            for (int c = stid; c < upr; c += kSgThreads) dst[c] = __ldg(src + c);
+          }
+        }
+        if (writer) {
+          for (int q = stid; q < kStepHash; q += kSgThreads) {
+            if (h_key[q] >= 0 && h_chg[q] >= 0) {
+              a.held[h_chg[q]] = s_bits[h_chg[q]];  // the ids holding a slot: the window's
+              const int sl = h_sold[q];             // a slot left free by an id that left
+              if (h_ent[q] == 0 && (unsigned)sl < (unsigned)W && ((s_fs[sl >> 5] >> (sl & 31)) & 1u))
+                a.slot_id[sl] = -1;
+            }
+          }
+          for (int r = stid; r < n_new; r += kSgThreads) {
+            const int sl = p_slot[r], id = p_id[r];
+            a.new_slot[r] = sl;
+            a.new_id[r] = id;
+            if (sl >= 0) {
+              a.slot_id[sl] = id;
+              a.slot_of[id] = sl;
+            }
+          }
+          for (int w = stid; w < fsw; w += kSgThreads) a.slot_free[w] = s_fs[w];
+          if (stid == 0) {
+            a.slot_meta[0] = s_misc[3];
+            a.slot_meta[1] = n_new;
+            *a.slot_len = len_new;
+          }
+        }
+      }
+    }
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   }
   tc_fence_before();
@@ -1056,11 +1312,14 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
 
 constexpr int kStepSizes[] = {8, 6, 5, 4};  // cluster sizes the one-launch step can take
 constexpr int kNumStepSizes = 4;
-int g_step_clusters[kNumStepSizes] = {0, 0, 0, 0};  // resident clusters of each size (prepare_step_kernel)
+// resident clusters of each size (prepare_step_kernel), of the canonical and
+// of the slot-stable variant
+int g_step_clusters[2][kNumStepSizes] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
 
-template <int CL>
+template <int CL, bool SLOTS>
 int prepare_one() {
-  cudaError_t e = cudaFuncSetAttribute(step_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+  cudaError_t e =
+      cudaFuncSetAttribute(step_kernel<CL, SLOTS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -1077,7 +1336,7 @@ int prepare_one() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, step_kernel<CL>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, step_kernel<CL, SLOTS>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     clusters = 0;
   }
@@ -1087,10 +1346,14 @@ int prepare_one() {
 }  // namespace
 
 cudaError_t prepare_step_kernel() {
-  g_step_clusters[0] = prepare_one<8>();
-  g_step_clusters[1] = prepare_one<6>();
-  g_step_clusters[2] = prepare_one<5>();
-  g_step_clusters[3] = prepare_one<4>();
+  g_step_clusters[0][0] = prepare_one<8, false>();
+  g_step_clusters[0][1] = prepare_one<6, false>();
+  g_step_clusters[0][2] = prepare_one<5, false>();
+  g_step_clusters[0][3] = prepare_one<4, false>();
+  g_step_clusters[1][0] = prepare_one<8, true>();
+  g_step_clusters[1][1] = prepare_one<6, true>();
+  g_step_clusters[1][2] = prepare_one<5, true>();
+  g_step_clusters[1][3] = prepare_one<4, true>();
   return cudaSuccess;
 }
 
@@ -1098,12 +1361,19 @@ cudaError_t prepare_step_kernel() {
 // items are the tiles of W_max rows plus the draft item; take
 // the cluster size that runs them with the fewest items per cluster, then the
 // largest (a smaller share of H per CTA), and just enough clusters.
-int step_plan(const Dims &d, int *tiles_per_cluster, int *cluster_size) {
+int step_plan(const Dims &d, bool slots, int *tiles_per_cluster, int *cluster_size) {
   const int items = (d.W_max + kUM - 1) / kUM + 1;
   int best_ncl = 0, best_tpc = 0, best_size = 0;
+  // the slot-stable variant keeps a copy of the slot table in the stage ring
+  if (slots && kCopyOff + 4 * round4(d.W_max) > kSRing) {
+    *tiles_per_cluster = 0;
+    *cluster_size = 0;
+    return 0;
+  }
   for (int i = 0; i < kNumStepSizes; ++i) {
     const int size = kStepSizes[i];
-    const int most = g_step_clusters[i] < kMaxStepCtas / size ? g_step_clusters[i] : kMaxStepCtas / size;
+    const int res = g_step_clusters[slots ? 1 : 0][i];
+    const int most = res < kMaxStepCtas / size ? res : kMaxStepCtas / size;
     if (most < 1) continue;
     const int tpc = (items + most - 1) / most;
     if (tpc > kMaxItemsPerCluster) continue;
@@ -1116,7 +1386,7 @@ int step_plan(const Dims &d, int *tiles_per_cluster, int *cluster_size) {
     // about as many CTAs as a full window would, where they are resident
     const int want = (kMinStepCtas + size - 1) / size;
     if (ncl < want) ncl = want < most ? want : most;
-    const StepSmem L = step_smem(d.nwords_pad, (d.W_max + 3) & ~3, d.W_max, ncl * size, d.K_ver);
+    const StepSmem L = step_smem(d.nwords_pad, (d.W_max + 3) & ~3, d.W_max, ncl * size, d.K_ver, slots);
     if (step_smem_bytes(L) > kMaxSmem) continue;
     if (best_ncl == 0 || tpc < best_tpc) {
       best_ncl = ncl;
@@ -1168,8 +1438,20 @@ cudaError_t launch_step(const StepLaunch &L, cudaStream_t st) {
   a.t_max = (L.d.W_max + kUM - 1) / kUM;
   a.vec = L.d.K_ver > 0 && (L.d.V % 4 == 0) && (reinterpret_cast<uintptr_t>(L.zrow) % 16 == 0);
   a.probe = L.probe ? 1 : 0;
+  if (L.slots) {
+    a.slot_id = L.s.slot_id;
+    a.slot_of = L.s.slot_of;
+    a.slot_free = L.s.slot_free;
+    a.held = L.s.held;
+    a.slot_meta = L.s.slot_meta;
+    a.new_slot = L.s.new_slot;
+    a.new_id = L.s.new_id;
+    a.slot_rows = L.s.slot_rows;
+    a.slot_len = L.s.slot_len;
+    a.fs_words = slot_words(L.d.W_max);
+  }
   const int P = L.clusters * L.cluster_size;
-  const StepSmem S = step_smem(L.d.nwords_pad, a.ring_words, L.d.W_max, P, L.d.K_ver);
+  const StepSmem S = step_smem(L.d.nwords_pad, a.ring_words, L.d.W_max, P, L.d.K_ver, L.slots);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)P);
   cfg.blockDim = dim3(kSThreads);
@@ -1180,11 +1462,20 @@ cudaError_t launch_step(const StepLaunch &L, cudaStream_t st) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (L.slots) {
+    switch (L.cluster_size) {
+      case 8: return cudaLaunchKernelEx(&cfg, step_kernel<8, true>, tmH, a);
+      case 6: return cudaLaunchKernelEx(&cfg, step_kernel<6, true>, tmH, a);
+      case 5: return cudaLaunchKernelEx(&cfg, step_kernel<5, true>, tmH, a);
+      case 4: return cudaLaunchKernelEx(&cfg, step_kernel<4, true>, tmH, a);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (L.cluster_size) {
-    case 8: return cudaLaunchKernelEx(&cfg, step_kernel<8>, tmH, a);
-    case 6: return cudaLaunchKernelEx(&cfg, step_kernel<6>, tmH, a);
-    case 5: return cudaLaunchKernelEx(&cfg, step_kernel<5>, tmH, a);
-    case 4: return cudaLaunchKernelEx(&cfg, step_kernel<4>, tmH, a);
+    case 8: return cudaLaunchKernelEx(&cfg, step_kernel<8, false>, tmH, a);
+    case 6: return cudaLaunchKernelEx(&cfg, step_kernel<6, false>, tmH, a);
+    case 5: return cudaLaunchKernelEx(&cfg, step_kernel<5, false>, tmH, a);
+    case 4: return cudaLaunchKernelEx(&cfg, step_kernel<4, false>, tmH, a);
     default: return cudaErrorInvalidValue;
   }
 }

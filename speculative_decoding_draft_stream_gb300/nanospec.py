@@ -36,6 +36,7 @@ EXPORTED = (
     "ns_gather_sub_lm_head_topk", "ns_trace_events", "ns_dense_lm_head_topk_noalloc", "ns_gather_new_head_rows",
     "ns_slot_lm_head_logits_topk", "ns_step_slots", "ns_get_slots", "ns_step_batch", "ns_sub_lm_head_indexed_topk",
     "ns_step_launches", "ns_step_batch_union", "ns_get_union", "ns_set_copy_ctas", "ns_step_host",
+    "ns_step_slots_fused",
 )
 NOALLOC_MAX_LOGITS = 1 << 20
 
@@ -69,6 +70,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "ns_destroy": (I32, [P]),
         "ns_device_bytes": (I64, [P]),
         "ns_step_launches": (I32, [P]),
+        "ns_step_slots_fused": (I32, [P, I32]),
         "ns_set_copy_ctas": (I32, [P, I32]),
         "ns_step_host": (I32, [P, I32, P, I32, P, U16P, P, I32, I32, P, P, P]),
         "ns_stream_init": (I32, [P, I32, P, I32, P, P]),
@@ -182,6 +184,10 @@ class Handle:
     def step_launches(self) -> int:
         """Kernel launches of one ns_step on this handle (1: the one-launch step)."""
         return int(self._lib.ns_step_launches(self._h))
+
+    def step_slots_fused(self, seq: int) -> int:
+        """1 when the next ns_step_slots on `seq` is one launch (the slot table matches the window)."""
+        return int(self._lib.ns_step_slots_fused(self._h, seq))
 
     # -- the C ABI -------------------------------------------------------------
     def stream_init(self, seq: int, prompt: Optional[torch.Tensor], prefill_logits: Optional[torch.Tensor],

@@ -72,7 +72,7 @@ def check_slot_projection(logits_dev, ids_dev, vals_dev, hid_bits, osl: oracle.O
     check_topk(ids_dev.cpu().numpy(), vals_dev.cpu().numpy(), want_by_I, I, k, tol)
 
 
-def _run(pkg, cfg: WorkloadConfig, fused: bool, steps=None, logit_steps=None):
+def _run(pkg, cfg: WorkloadConfig, fused: bool, steps=None, logit_steps=None, one_launch=False):
     wl = Workload(cfg)
     W = wl.w_head()
     W_dev = dev_bf16(W)
@@ -99,6 +99,8 @@ def _run(pkg, cfg: WorkloadConfig, fused: bool, steps=None, logit_steps=None):
             tree_d, hid_d = dev_i32(trees[t]), dev_bf16(hid)
             vb_d = dev_f32(vb) if vb is not None else None
             if fused:
+                if one_launch:  # the table matches the window: ns_step_slots is the one-launch kernel
+                    assert h.step_slots_fused(seq) == 1
                 ids, vals = h.step_slots(seq, tree_d, vb_d, vr, W_dev, hid_d, cfg.k, logits=logits)
             else:
                 h.state_update(seq, tree_d, vb_d, vr)
@@ -136,14 +138,63 @@ EDGE = [
 @pytest.mark.parametrize("fused", [False, True], ids=["separate_calls", "step_slots"])
 @pytest.mark.parametrize("cfg", [TOY, MID, WIDE] + EDGE, ids=lambda c: c.name)
 def test_slots_every_step(pkg, cfg, fused):
-    _run(pkg, cfg, fused)
+    _run(pkg, cfg, fused, one_launch=fused and cfg in (TOY, MID, WIDE))
 
 
 def test_slots_full_size_llama(pkg):
     """The Llama-3-8B-shaped head (V=128256, H=4096, W_max=3072): slot state
-    on 40 steps, logits and top-k on a sample of them."""
+    on 40 one-launch steps, logits and top-k on a sample of them."""
     cfg = get_config("llama3_8b_v128256_h4096")
-    _run(pkg, cfg, True, steps=40, logit_steps={0, 1, 2, 3, 17, 39})
+    _run(pkg, cfg, True, steps=40, logit_steps={0, 1, 2, 3, 17, 39}, one_launch=True)
+
+
+def test_step_slots_paths_interleave(pkg):
+    """ns_step_slots is one launch only while the slot table matches the
+    window: a canonical step, an append with a rebuild, or a state update in
+    between send it down the multi-launch chain once, which puts the table
+    back in step.  Every step of the mix is checked against the oracle."""
+    cfg = MID
+    wl = Workload(cfg)
+    W = wl.w_head()
+    W_dev = dev_bf16(W)
+    # what runs at each step: the slot step, or a window change without a slot update first
+    plan = ["slots", "slots", "step", "slots", "slots", "append", "slots", "update", "slots", "slots", "slots",
+            "slots"]
+    assert len(plan) <= cfg.steps
+    with _handle(pkg, cfg, wl.prompt_len(0)) as h:
+        ost = oracle.OracleStream(cfg.V, cfg.W_max, cfg.K_pre, cfg.K_ver)
+        osl = oracle.OracleSlots(cfg.W_max, cfg.H)
+        prompt, Z = wl.prompt(0), wl.prefill_logits(0)
+        ost.init(prompt, Z)
+        h.stream_init(0, dev_i32(prompt), dev_f32(Z))
+        h.build_active_vocab(0)
+        assert h.step_slots_fused(0) == 0  # the table is empty, the window is not
+        trees = wl.trees(0)
+        logits = torch.zeros((cfg.n_tree, cfg.W_max), dtype=torch.float32, device="cuda")
+        for t, what in enumerate(plan):
+            vb, vr, hid = wl.verify_logits(0, t), wl.verify_row(0, t), wl.hiddens(0, t)
+            tree_d, vb_d, hid_d = dev_i32(trees[t]), dev_f32(vb), dev_bf16(hid)
+            ost.append(trees[t], vb, vr)
+            if what == "slots":
+                expect = 0 if t == 0 or plan[t - 1] != "slots" else 1
+                assert h.step_slots_fused(0) == expect, (t, what)
+                ids, vals = h.step_slots(0, tree_d, vb_d, vr, W_dev, hid_d, cfg.k, logits=logits)
+                assert h.step_slots_fused(0) == 1
+                I = check_state(h, 0, ost, full=False)
+                pairs = osl.update(I, W)
+                check_slots(h, 0, osl, pairs, W)
+                check_slot_projection(logits, ids, vals, hid, osl, I, cfg.k)
+            else:
+                if what == "step":
+                    h.step(0, tree_d, vb_d, vr, W_dev, hid_d, cfg.k)
+                elif what == "append":
+                    h.stream_append(0, tree_d, vb_d, vr)
+                    h.build_active_vocab(0)
+                else:
+                    h.state_update(0, tree_d, vb_d, vr)
+                assert h.step_slots_fused(0) == 0, (t, what)
+                check_state(h, 0, ost, full=False)
+        assert h.get_error() == 0
 
 
 def test_slots_follow_any_update_schedule(pkg):
