@@ -837,16 +837,27 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
         for (int c0 = 0; c0 < m_act; c0 += 8 * kKThreads) {
           uint32_t hk[8], hi[8];
           const int j0 = c0 + 8 * tid;
-          if (vec_l && j0 + 8 <= m_act) {
-            const float4 f0 = __ldcg(reinterpret_cast<const float4 *>(row + j0));
-            const float4 f1 = __ldcg(reinterpret_cast<const float4 *>(row + j0 + 4));
-            const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+          // every lane takes the same path (a lane that straddles m_act
+          // would otherwise wait for a second round of loads): 16-byte
+          // groups that start below m_act (inside the row: m_act <= W_max <=
+          // ld, both groups and ld multiples of four), then a mask
+          float v[8];
+          if (vec_l) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) hk[q] = order_key(v[q]);
+            for (int h2 = 0; h2 < 2; ++h2) {
+              float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (j0 + 4 * h2 < m_act) f = __ldcg(reinterpret_cast<const float4 *>(row + j0 + 4 * h2));
+              v[4 * h2] = f.x;
+              v[4 * h2 + 1] = f.y;
+              v[4 * h2 + 2] = f.z;
+              v[4 * h2 + 3] = f.w;
+            }
           } else {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) hk[q] = j0 + q < m_act ? order_key(__ldcg(row + j0 + q)) : 0u;
+            for (int q = 0; q < 8; ++q) v[q] = j0 + q < m_act ? __ldcg(row + j0 + q) : 0.f;
           }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) hk[q] = j0 + q < m_act ? order_key(v[q]) : 0u;
           if (kSlots) {  // slot-stable: rank by (value, id), the id from the slot table
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
