@@ -481,7 +481,13 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
     if (nsl < 0) nsl = 0;
   }
   constexpr int kPass = 8 * kSgThreads;
-  float x[8];
+  constexpr int kFold = 4;  // extra values a thread can fold into the one pass
+  // With K_ver <= 8 a thread's values beyond its 8 best never reach the
+  // Top-K, so a slice up to kFold values per thread longer than a pass is
+  // ranked in one pass: the extra values (loaded with the pass) replace a
+  // thread's worst.
+  const bool fold = K <= 8 && nsl > kPass && nsl <= kPass + kFold * kSgThreads;
+  float x[8], xe[kFold];
   auto load_pass = [&](int c0) {
     const int n = nsl - c0;
     if (a.vec) {
@@ -501,9 +507,27 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
       }
     }
   };
+  auto load_extra = [&]() {
+#pragma unroll
+    for (int q = 0; q < kFold; ++q) xe[q] = __int_as_float(0x7fffffff);
+    if (a.vec) {
+      const int e = kPass + 4 * stid;
+      if (e < nsl) {
+        const float4 f = ld_stream_f4(a.zrow + lo + e);
+        xe[0] = f.x, xe[1] = f.y, xe[2] = f.z, xe[3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kFold; ++q) {
+        const int e = kPass + q * kSgThreads + stid;
+        if (e < nsl) xe[q] = ld_stream_f32(a.zrow + lo + e);
+      }
+    }
+  };
   int tree_id = 0;
   if (sgrp) {
     if (nsl > 0) load_pass(0);
+    if (fold) load_extra();
     tree_id = stid < n_tree ? a.tree[stid] : 0;
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -981,7 +1005,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
       wl_k[kSgWarps * K + stid] = 0u;  // the running Top-K starts empty
       wl_i[kSgWarps * K + stid] = (uint32_t)kEmptyId;
     }
-    for (int c0 = 0; c0 < nsl; c0 += kPass) {
+    for (int c0 = 0; c0 < (fold ? kPass : nsl); c0 += kPass) {
       if (c0 > 0) load_pass(c0);
       uint32_t hk[8], hi[8];
 #pragma unroll
@@ -989,6 +1013,24 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
         const int e = a.vec ? 4 * ((q >> 2) * kSgThreads + stid) + (q & 3) : q * kSgThreads + stid;
         hk[q] = order_key(x[q]);  // padding is NaN: key 0, never ranks
         hi[q] = hk[q] != 0u ? (uint32_t)(lo + c0 + e) : (uint32_t)kEmptyId;
+      }
+      if (fold) {  // each extra value replaces this thread's worst entry when better
+#pragma unroll
+        for (int f = 0; f < kFold; ++f) {
+          const int e = a.vec ? kPass + 4 * stid + f : kPass + f * kSgThreads + stid;
+          const uint32_t ek = order_key(xe[f]);
+          const uint32_t ei = ek != 0u ? (uint32_t)(lo + e) : (uint32_t)kEmptyId;
+          int w = 0;  // the worst entry: smallest key, then largest id
+          uint32_t wk = hk[0], wi = hi[0];
+#pragma unroll
+          for (int q = 1; q < 8; ++q)
+            if (hk[q] < wk || (hk[q] == wk && hi[q] > wi)) w = q, wk = hk[q], wi = hi[q];
+          if (ek > wk || (ek == wk && ei < wi)) {
+#pragma unroll
+            for (int z = 0; z < 8; ++z)
+              if (z == w) hk[z] = ek, hi[z] = ei;
+          }
+        }
       }
       uint32_t wk, wi;
       warp_topk8_lanes(hk, hi, K, &wk, &wi);
@@ -1197,21 +1239,40 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kSThreads, 1)
         if (stid == 0) mbar_arrive(bar_state);  // the tile and verify groups may place their columns
       }
 
-      // compaction: per 4-word group, the number of ids before it
+      // compaction: per 4-word group, the number of ids before it.  State
+      // warp w scans the groups [w * C, (w + 1) * C), 32 consecutive groups
+      // per round (one per lane: conflict-free 16-byte reads, a shuffle scan
+      // per round), then adds the warps before it.
       const int ng = a.nwords_pad / 4;
-      const int G = (ng + kSgThreads - 1) / kSgThreads;
+      const int C = (((ng + kSgWarps - 1) / kSgWarps) + kWarp - 1) & ~(kWarp - 1);
+      const int g0 = swarp * C;
       const uint4 *b4 = reinterpret_cast<const uint4 *>(s_bits);
-      int cnt = 0;
-      for (int g = stid * G; g < stid * G + G && g < ng; ++g) {
-        const uint4 w4 = b4[g];
-        cnt += __popc(w4.x) + __popc(w4.y) + __popc(w4.z) + __popc(w4.w);
+      int wtot = 0;
+#pragma unroll 4
+      for (int c0 = 0; c0 < C; c0 += kWarp) {
+        const int g = g0 + c0 + lane;
+        int cnt = 0;
+        if (g < ng) {
+          const uint4 w4 = b4[g];
+          cnt = __popc(w4.x) + __popc(w4.y) + __popc(w4.z) + __popc(w4.w);
+        }
+        const int incl = warp_inclusive_scan(cnt);
+        if (g < ng) s_goff[g] = wtot + incl - cnt;
+        wtot += __shfl_sync(0xffffffffu, incl, kWarp - 1);
       }
-      int total;
-      int off = sg_exclusive_scan(cnt, sh_scan, &total);
-      for (int g = stid * G; g < stid * G + G && g < ng; ++g) {
-        s_goff[g] = off;
-        const uint4 w4 = b4[g];
-        off += __popc(w4.x) + __popc(w4.y) + __popc(w4.z) + __popc(w4.w);
+      if (lane == 0) sh_scan[swarp] = wtot;
+      named_sync(kBarS, kSgThreads);
+      int woff = 0, total = 0;
+#pragma unroll
+      for (int q = 0; q < kSgWarps; ++q) {
+        if (q < swarp) woff += sh_scan[q];
+        total += sh_scan[q];
+      }
+      if (woff != 0) {
+        for (int c0 = 0; c0 < C; c0 += kWarp) {
+          const int g = g0 + c0 + lane;
+          if (g < ng) s_goff[g] += woff;
+        }
       }
       m_act = total < W ? total : W;
       if (!kSlots && stid == 0) s_misc[3] = m_act;
