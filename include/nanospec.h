@@ -469,6 +469,35 @@ NS_API ns_status ns_get_state(ns_handle *h, int32_t seq, const int32_t **ring, c
                        const uint32_t **counts);
 
 /*
+ * Checkpoint and resume of one sequence's stream state (not on the pages:
+ * the state is the last W_max stream entries and |S|, everything else
+ * follows from them).  The checkpoint is a 32-byte header (magic "NSST",
+ * version 1, V, W_max, |S| as int64, n = min(|S|, W_max), 4 bytes reserved;
+ * little-endian) followed by the window's n entries (int32), oldest first.
+ *
+ * ns_state_export_bytes: the largest checkpoint of this handle (header +
+ * 4 * W_max bytes); 0 for NULL.
+ *
+ * ns_state_export writes the checkpoint of `seq` to host_buf (buf_bytes
+ * long; NS_ERR_ARG when too short) and its size to *written; with host_buf
+ * NULL it only writes the size.  It synchronises `stream` (the state is
+ * read after the work queued on it).  NS_ERR_STATE before ns_stream_init.
+ *
+ * ns_state_import makes `seq` continue from a checkpoint: as ns_stream_init
+ * it resets the sequence, then restores the ring and |S|, recounts the
+ * window (counts, bitmap) and builds I_t, on `stream`.  The packed buffer is
+ * not restored (the next ns_step or ns_gather_head_rows fills it) and the
+ * slot table starts empty.  The host buffer is read before the call returns
+ * (the call waits for the work queued on `stream` before its copy).
+ * NS_ERR_ARG for a checkpoint of another V or W_max, a wrong magic, version
+ * or size, or an id outside [0, V).
+ */
+NS_API int64_t ns_state_export_bytes(const ns_handle *h);
+NS_API ns_status ns_state_export(ns_handle *h, int32_t seq, void *host_buf, int64_t buf_bytes, int64_t *written,
+                                 ns_stream stream);
+NS_API ns_status ns_state_import(ns_handle *h, int32_t seq, const void *host_buf, int64_t bytes, ns_stream stream);
+
+/*
  * Device pointers to a sequence's slot buffer (owned by the handle).  Any
  * out-pointer may be NULL.
  *   slot_id    int32 [W_max]  id held by each slot, -1 = free

@@ -797,6 +797,86 @@ ns_status ns_get_state(ns_handle *h, int32_t seq, const int32_t **ring, const in
   return NS_OK;
 }
 
+// Checkpoint of one sequence (little-endian): a 32-byte header, then the
+// window's stream entries oldest first.
+namespace {
+constexpr char kCkptMagic[4] = {'N', 'S', 'S', 'T'};
+constexpr uint32_t kCkptVersion = 1;
+struct CkptHeader {
+  char magic[4];
+  uint32_t version;
+  int32_t V, W_max;
+  int64_t length;  // |S|
+  int32_t n;       // entries that follow: min(|S|, W_max)
+  int32_t reserved;
+};
+static_assert(sizeof(CkptHeader) == 32, "checkpoint header layout");
+}  // namespace
+
+int64_t ns_state_export_bytes(const ns_handle *h) {
+  return h ? (int64_t)sizeof(CkptHeader) + 4 * (int64_t)h->cfg.W_max : 0;
+}
+
+ns_status ns_state_export(ns_handle *h, int32_t seq, void *host_buf, int64_t buf_bytes, int64_t *written,
+                          ns_stream stream) {
+  if (!valid_seq(h, seq) || !written) return NS_ERR_ARG;
+  if (!h->inited[seq]) return NS_ERR_STATE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const ns::SeqDev &s = h->seqs[seq];
+  const int W = h->cfg.W_max;
+  long long len[2] = {0, 0};
+  std::vector<int32_t> ring((size_t)W);
+  cudaError_t e = cudaMemcpyAsync(len, s.length, sizeof(len), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ring.data(), s.ring, (size_t)W * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_status(e);
+  const long long n = len[0] < W ? len[0] : W;
+  const int64_t need = (int64_t)sizeof(CkptHeader) + 4 * n;
+  *written = need;
+  if (!host_buf) return NS_OK;  // the size only
+  if (buf_bytes < need) return NS_ERR_ARG;
+  CkptHeader hd{};
+  std::memcpy(hd.magic, kCkptMagic, 4);
+  hd.version = kCkptVersion;
+  hd.V = h->cfg.V;
+  hd.W_max = W;
+  hd.length = len[0];
+  hd.n = (int32_t)n;
+  char *out = static_cast<char *>(host_buf);
+  std::memcpy(out, &hd, sizeof(hd));
+  int32_t *ent = reinterpret_cast<int32_t *>(out + sizeof(hd));
+  for (long long i = 0; i < n; ++i) {
+    const int32_t x = ring[(size_t)((len[0] - n + i) % W)];
+    std::memcpy(ent + i, &x, 4);
+  }
+  return NS_OK;
+}
+
+ns_status ns_state_import(ns_handle *h, int32_t seq, const void *host_buf, int64_t bytes, ns_stream stream) {
+  if (!valid_seq(h, seq) || !host_buf || bytes < (int64_t)sizeof(CkptHeader)) return NS_ERR_ARG;
+  CkptHeader hd;
+  std::memcpy(&hd, host_buf, sizeof(hd));
+  const int W = h->cfg.W_max;
+  if (std::memcmp(hd.magic, kCkptMagic, 4) != 0 || hd.version != kCkptVersion || hd.V != h->cfg.V ||
+      hd.W_max != W || hd.length < 0 || hd.n < 0 || hd.n != (hd.length < W ? hd.length : W) ||
+      bytes < (int64_t)sizeof(CkptHeader) + 4 * (int64_t)hd.n)
+    return NS_ERR_ARG;
+  const char *in = static_cast<const char *>(host_buf) + sizeof(hd);
+  std::vector<int32_t> ring((size_t)W, 0);
+  for (int i = 0; i < hd.n; ++i) {
+    int32_t x;
+    std::memcpy(&x, in + 4 * (size_t)i, 4);
+    if (x < 0 || x >= h->cfg.V) return NS_ERR_ARG;
+    ring[(size_t)((hd.length - hd.n + i) % W)] = x;
+  }
+  // the copy from this pageable vector is staged before cudaMemcpyAsync returns
+  const cudaError_t e =
+      ns::launch_restore(h->seqs[seq], h->dims, ring.data(), hd.length, h->err, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) h->inited[seq] = 1;
+  h->slots_synced[seq] = 0;  // the slot table restarts empty
+  return cuda_status(e);
+}
+
 ns_status ns_get_slots(ns_handle *h, int32_t seq, const int32_t **slot_id, const int32_t **meta,
                        const int32_t **new_slots, const int32_t **new_ids, const uint16_t **rows) {
   if (!valid_seq(h, seq)) return NS_ERR_ARG;

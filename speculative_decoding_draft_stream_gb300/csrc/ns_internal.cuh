@@ -440,6 +440,12 @@ cudaError_t launch_append_batch(const SeqDev &s, const Dims &d, int nseq, const 
 // Sets the state kernels' shared-memory limits and picks d->state_cluster.
 cudaError_t prepare_state_kernels(Dims *d);
 cudaError_t launch_build(const SeqDev &s, const Dims &d, uint32_t *err, cudaStream_t st);
+// A restored checkpoint: resets the sequence (as ns_stream_init), copies the
+// ring image h_ring [W_max] (host memory; the window's entries at their ring
+// slots), counts the window into the counts and bitmap, sets |S| = len and
+// builds I_t.
+cudaError_t launch_restore(const SeqDev &s, const Dims &d, const int32_t *h_ring, long long len, uint32_t *err,
+                           cudaStream_t st);
 // out[w] = OR over sequences b < nseq of sequence b's bitmap word w (sequence
 // b's state is b * seq_bytes past s's).
 cudaError_t launch_union_bitmap(const SeqDev &s, const Dims &d, int nseq, long long seq_bytes, uint32_t *out,

@@ -261,6 +261,27 @@ __global__ void __launch_bounds__(kStateThreads) init_compose_kernel(SeqDev s, D
   }
 }
 
+// The window counts and bitmap of a ring written by the host (a restored
+// checkpoint): positions [|S| - min(|S|, W_max), |S|) hold the window, which
+// this counts as init_compose_kernel does; then |S| and its ring slot.
+__global__ void restore_window_kernel(SeqDev s, Dims d, long long len, uint32_t *err) {
+  const long long start = len > d.W_max ? len - d.W_max : 0;
+  for (long long p = start + blockIdx.x * (long long)blockDim.x + threadIdx.x; p < len;
+       p += (long long)gridDim.x * blockDim.x) {
+    const int x = s.ring[p % d.W_max];
+    if ((unsigned)x >= (unsigned)d.V) {  // the host checked every entry
+      set_flag(err, NS_FLAG_BAD_ID);
+      continue;
+    }
+    atomicAdd(&s.counts[x], 1u);
+    atomicOr(&s.bitmap[x >> 5], 1u << (x & 31));
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    s.length[0] = len;
+    s.length[1] = len % d.W_max;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Decode-step append (+ optional compaction): one cluster of 16 CTAs (8 where
 // the device cannot hold 16)
@@ -883,6 +904,22 @@ cudaError_t launch_append_batch(const SeqDev &s, const Dims &d, int nseq, const 
   const bool vec = d.K_ver > 0 && (d.V % 4 == 0) && (reinterpret_cast<uintptr_t>(verify) % 16 == 0);
   return vec ? launch_append_k<true, true, true>(s, d, tree, n_tree, verify, err, st, bt, nseq, cluster)
              : launch_append_k<false, true, true>(s, d, tree, n_tree, verify, err, st, bt, nseq, cluster);
+}
+
+cudaError_t launch_restore(const SeqDev &s, const Dims &d, const int32_t *h_ring, long long len, uint32_t *err,
+                           cudaStream_t st) {
+  const int n = reset_extent(d);
+  init_reset_kernel<<<(n + 255) / 256, 256, 0, st>>>(s, d);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(s.ring, h_ring, (size_t)d.W_max * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return e;
+  const long long win = len < d.W_max ? len : d.W_max;
+  const int blocks = win > 0 ? (int)((win + 255) / 256) : 1;
+  restore_window_kernel<<<blocks, 256, 0, st>>>(s, d, len, err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_build(s, d, err, st);
 }
 
 cudaError_t launch_build(const SeqDev &s, const Dims &d, uint32_t *err, cudaStream_t st) {

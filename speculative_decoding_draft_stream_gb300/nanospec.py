@@ -36,7 +36,7 @@ EXPORTED = (
     "ns_gather_sub_lm_head_topk", "ns_trace_events", "ns_dense_lm_head_topk_noalloc", "ns_gather_new_head_rows",
     "ns_slot_lm_head_logits_topk", "ns_step_slots", "ns_get_slots", "ns_step_batch", "ns_sub_lm_head_indexed_topk",
     "ns_step_launches", "ns_step_batch_union", "ns_get_union", "ns_set_copy_ctas", "ns_step_host",
-    "ns_step_slots_fused",
+    "ns_step_slots_fused", "ns_state_export_bytes", "ns_state_export", "ns_state_import",
 )
 NOALLOC_MAX_LOGITS = 1 << 20
 
@@ -71,6 +71,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "ns_device_bytes": (I64, [P]),
         "ns_step_launches": (I32, [P]),
         "ns_step_slots_fused": (I32, [P, I32]),
+        "ns_state_export_bytes": (I64, [P]),
+        "ns_state_export": (I32, [P, I32, P, I64, ctypes.POINTER(I64), P]),
+        "ns_state_import": (I32, [P, I32, P, I64, P]),
         "ns_set_copy_ctas": (I32, [P, I32]),
         "ns_step_host": (I32, [P, I32, P, I32, P, U16P, P, I32, I32, P, P, P]),
         "ns_stream_init": (I32, [P, I32, P, I32, P, P]),
@@ -184,6 +187,20 @@ class Handle:
     def step_launches(self) -> int:
         """Kernel launches of one ns_step on this handle (1: the one-launch step)."""
         return int(self._lib.ns_step_launches(self._h))
+
+    def state_export(self, seq: int, stream=None) -> bytes:
+        """The checkpoint of `seq` (synchronises the stream)."""
+        n = self._lib.ns_state_export_bytes(self._h)
+        buf = ctypes.create_string_buffer(int(n))
+        written = ctypes.c_int64(0)
+        _check(self._lib.ns_state_export(self._h, seq, buf, n, ctypes.byref(written), _stream(stream)),
+               "ns_state_export")
+        return buf.raw[: written.value]
+
+    def state_import(self, seq: int, data: bytes, stream=None) -> None:
+        """Continue `seq` from a checkpoint made by state_export."""
+        buf = ctypes.create_string_buffer(bytes(data), len(data))
+        _check(self._lib.ns_state_import(self._h, seq, buf, len(data), _stream(stream)), "ns_state_import")
 
     def step_slots_fused(self, seq: int) -> int:
         """1 when the next ns_step_slots on `seq` is one launch (the slot table matches the window)."""
