@@ -308,15 +308,17 @@ NS_API ns_status ns_sub_lm_head_indexed_topk(ns_handle *h, int32_t seq, const ui
 NS_API ns_status ns_set_copy_ctas(ns_handle *h, int32_t ctas);
 
 /*
- * ns_step with the step's inputs and outputs in host memory: on `stream` it
- * copies the tree ids (int32 [n_tree]), the verify row (fp32 [V], ignored
- * when K_ver = 0) and the hidden rows (bf16 [n x H]) into the handle's
- * device staging buffers, runs ns_step on them (logits in the handle's
- * scratch), and copies the top-k ids and values (int32 / fp32 [n x k]) back
- * to h_topk_ids / h_topk_vals.  It returns once everything is enqueued; the
- * outputs are valid after the stream synchronises.  Host buffers should be
- * pinned (page-locked) for the copies to run asynchronously; they must stay
- * valid until then.  d_W_head is device memory as in ns_step.  With trace
+ * ns_step with the step's inputs and outputs in host memory: the tree ids
+ * (int32 [n_tree]), the verify row (fp32 [V], ignored when K_ver = 0) and
+ * the hidden rows (bf16 [n x H]) in, the top-k ids and values (int32 / fp32
+ * [n x k]) out to h_topk_ids / h_topk_vals, all on `stream` (logits in the
+ * handle's scratch).  Page-locked buffers that the device can address (the
+ * tree ids, the verify row, the outputs) are read and written by the step
+ * kernel in place; other buffers, and always the hidden rows, go through
+ * the handle's device staging by copies.  It returns once everything is
+ * enqueued; the outputs are valid after the stream synchronises, and every
+ * buffer must stay valid until then.  Pinned buffers also let the copies run
+ * asynchronously.  d_W_head is device memory as in ns_step.  With trace
  * events set (ns_trace_events) the four events bracket the input copies,
  * the step and the output copies.  Arguments as in ns_step.
  */

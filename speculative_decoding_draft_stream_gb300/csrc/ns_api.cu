@@ -484,6 +484,18 @@ static cudaError_t enqueue_step(ns_handle *h, int32_t seq, const int32_t *d_tree
   return e;
 }
 
+// The device address of a page-locked host buffer the device can reach, or
+// null (pageable memory, or a null pointer).
+static void *device_view(const void *p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 ns_status ns_step_host(ns_handle *h, int32_t seq, const int32_t *h_tree_ids, int32_t n_tree,
                        const float *h_verify_row, const uint16_t *d_W_head, const uint16_t *h_hidden, int32_t n,
                        int32_t k, int32_t *h_topk_ids, float *h_topk_vals, ns_stream stream) {
@@ -496,20 +508,36 @@ ns_status ns_step_host(ns_handle *h, int32_t seq, const int32_t *h_tree_ids, int
   if (st != NS_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const bool tr = h->tracing;
+  // Page-locked host buffers that the device can address are read (tree ids,
+  // verify row) and written (top-k) by the step kernel in place, over the
+  // host link; other host buffers go through the device staging.  The
+  // hidden rows are always staged: the kernel reads them by TMA.
+  const int32_t *tree_d = reinterpret_cast<const int32_t *>(device_view(h_tree_ids));
+  const float *verify_d = reinterpret_cast<const float *>(device_view(h_verify_row));
+  int32_t *ids_d = reinterpret_cast<int32_t *>(device_view(h_topk_ids));
+  float *vals_d = reinterpret_cast<float *>(device_view(h_topk_vals));
+  const bool out_direct = ids_d != nullptr && vals_d != nullptr;
   cudaError_t e = tr ? trace_record(h->trace[0], cs) : cudaSuccess;
-  if (e == cudaSuccess && n_tree > 0)
+  if (e == cudaSuccess && n_tree > 0 && !tree_d) {
     e = cudaMemcpyAsync(h->st_tree, h_tree_ids, (size_t)n_tree * 4, cudaMemcpyHostToDevice, cs);
-  if (e == cudaSuccess && h->cfg.K_ver > 0)
+    tree_d = h->st_tree;
+  }
+  if (e == cudaSuccess && h->cfg.K_ver > 0 && !verify_d) {
     e = cudaMemcpyAsync(h->st_verify, h_verify_row, (size_t)h->cfg.V * 4, cudaMemcpyHostToDevice, cs);
+    verify_d = h->st_verify;
+  }
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(h->st_hidden, h_hidden, (size_t)n * h->cfg.H * 2, cudaMemcpyHostToDevice, cs);
   if (e == cudaSuccess && tr) e = trace_record(h->trace[1], cs);
   if (e == cudaSuccess)
-    e = enqueue_step(h, seq, h->st_tree, n_tree, h->st_verify, 0, d_W_head, h->st_hidden, n, k, nullptr, 0,
-                     h->st_ids, h->st_vals, cs, false);
+    e = enqueue_step(h, seq, n_tree > 0 ? tree_d : h->st_tree, n_tree, verify_d ? verify_d : h->st_verify, 0,
+                     d_W_head, h->st_hidden, n, k, nullptr, 0, out_direct ? ids_d : h->st_ids,
+                     out_direct ? vals_d : h->st_vals, cs, false);
   if (e == cudaSuccess && tr) e = trace_record(h->trace[2], cs);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(h_topk_ids, h->st_ids, (size_t)n * k * 4, cudaMemcpyDeviceToHost, cs);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(h_topk_vals, h->st_vals, (size_t)n * k * 4, cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess && !out_direct)
+    e = cudaMemcpyAsync(h_topk_ids, h->st_ids, (size_t)n * k * 4, cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess && !out_direct)
+    e = cudaMemcpyAsync(h_topk_vals, h->st_vals, (size_t)n * k * 4, cudaMemcpyDeviceToHost, cs);
   if (e == cudaSuccess && tr) e = trace_record(h->trace[3], cs);
   return cuda_status(e);
 }

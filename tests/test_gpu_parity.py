@@ -405,10 +405,15 @@ def test_trace_events_bracket_the_step(pkg):
         assert h._lib.ns_trace_events(h._h, None, 3) == -1  # wrong event count
 
 
-def test_step_host_equals_step(pkg):
-    """ns_step_host (inputs and outputs in pinned host memory, copies on the
-    stream) gives ns_step's window, I_t and top-k, bit for bit, on every step."""
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_step_host_equals_step(pkg, pinned):
+    """ns_step_host (inputs and outputs in host memory: pinned buffers read and
+    written in place by the kernel, pageable ones through copies) gives
+    ns_step's window, I_t and top-k, bit for bit, on every step."""
     cfg = MID
+
+    def host(t):
+        return t.pin_memory() if pinned else t.clone()
     wl = Workload(cfg)
     W_dev = dev_bf16(wl.w_head())
     k = cfg.k
@@ -417,14 +422,16 @@ def test_step_host_equals_step(pkg):
         for h in (ha, hb):
             h.stream_init(0, dev_i32(prompt), dev_f32(Z))
             h.build_active_vocab(0)
-        ids_h = torch.empty((cfg.n_tree, k), dtype=torch.int32).pin_memory()
-        vals_h = torch.empty((cfg.n_tree, k), dtype=torch.float32).pin_memory()
+        ids_h = host(torch.empty((cfg.n_tree, k), dtype=torch.int32))
+        vals_h = host(torch.empty((cfg.n_tree, k), dtype=torch.float32))
         for t in range(cfg.steps):
             tree, vb, vr, hid = wl.trees(0)[t], wl.verify_logits(0, t), wl.verify_row(0, t), wl.hiddens(0, t)
             ids_b, vals_b = hb.step(0, dev_i32(tree), dev_f32(vb), vr, W_dev, dev_bf16(hid), k)
-            ha.step_host(0, torch.from_numpy(np.ascontiguousarray(tree)).pin_memory(),
-                         torch.from_numpy(np.ascontiguousarray(vb[vr])).pin_memory(), W_dev,
-                         torch.from_numpy(np.ascontiguousarray(hid).view(np.int16)).pin_memory(), k, ids_h, vals_h)
+            # the host inputs stay alive until the stream has passed the step
+            tree_h = host(torch.from_numpy(np.ascontiguousarray(tree)))
+            verify_h = host(torch.from_numpy(np.ascontiguousarray(vb[vr])))
+            hid_h = host(torch.from_numpy(np.ascontiguousarray(hid).view(np.int16)))
+            ha.step_host(0, tree_h, verify_h, W_dev, hid_h, k, ids_h, vals_h)
             torch.cuda.synchronize()
             assert torch.equal(ids_h, ids_b.cpu()), f"step {t}: top-k ids"
             assert torch.equal(vals_h, vals_b.cpu()), f"step {t}: top-k values"
