@@ -680,10 +680,11 @@ def run_ours(args):
                 "timing": "CUDA events around each launch in a traced replay of the same steps"}
 
     # ---- end to end through the C ABI with host buffers ------------------------
-    # ns_step_host: one call per step copies the step's inputs (tree ids, the
-    # verify row, the draft hiddens) from pinned host memory, runs the step
-    # and copies the top-k ids and values back, all on the stream; the host
-    # then waits for the stream.  A second, traced pass splits the time.
+    # ns_step_host: one call per step takes the step's inputs (tree ids, the
+    # verify row, the draft hiddens) from pinned host memory and returns the
+    # top-k ids and values there, all on the stream (the hiddens by a copy,
+    # the rest read and written by the step kernel in place); the host then
+    # waits for the stream.  A second, traced pass splits the time.
     init()
     tree_p = [torch.from_numpy(np.ascontiguousarray(trees_h[u])).pin_memory() for u in range(T)]
     ver_p = [torch.from_numpy(np.ascontiguousarray(verify_h[u][vrows[u]])).pin_memory() for u in range(T)]
